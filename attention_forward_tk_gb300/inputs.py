@@ -1,0 +1,101 @@
+"""Seeded synthetic inputs for the attention forward workloads.
+
+This module only draws random numbers and rounds them to bf16; it holds no
+attention arithmetic, so the CUDA path and the CPU oracle can both be fed from
+it without sharing any part of the method.
+
+Workloads (the five problem shapes the library is measured and checked on):
+
+  name            B   H   N      D    mask     values
+  n256_d64        1   1   256    64   none     Q, K, V ~ N(0, 1)
+  n1024_d64       16  16  1024   64   none     Q, K, V ~ N(0, 1)
+  n4096_d128      16  16  4096   128  none     Q, K, V ~ N(0, 1)
+  n8192_d128_c    8   16  8192   128  causal   Q, K, V ~ N(0, 1)
+  n16384_d128_c   4   32  16384  128  causal   Q, K ~ 4 N(0, 1);
+                                               V ~ Student-t(3), clipped to +-8
+
+The scale is 1/sqrt(D) in every workload (the kernel examples on the pages use
+1/sqrt(64) = 0.125 and 1/sqrt(128) ~= 0.08838834764).
+
+Recipe: a CPU ``torch.Generator`` seeded with the workload's index (0..4) draws
+Q, then K, then V, in float32, with the shape [B, H, N, D]; scaling (4 N(0,1))
+and clipping happen in float32 before one round-to-nearest-even conversion to
+bfloat16.  A Student-t(3) draw is z / sqrt((z1^2 + z2^2 + z3^2) / 3) with all
+four normals from the same generator (z first, then a [..., 3] block).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    D: int
+    causal: bool
+    dist: str  # "normal" or "peaky_t3"
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def shape(self):
+        return (self.B, self.H, self.N, self.D)
+
+    @property
+    def flops(self) -> float:
+        """4*B*H*N^2*D, halved under the causal mask."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.D
+        return f / 2 if self.causal else f
+
+    @property
+    def io_bytes(self) -> int:
+        """Q, K, V read and O written in bf16, LSE written in fp32."""
+        elems = self.B * self.H * self.N * self.D
+        return 4 * elems * 2 + self.B * self.H * self.N * 4
+
+
+WORKLOADS = (
+    Workload("n256_d64", 1, 1, 256, 64, False, "normal", 0),
+    Workload("n1024_d64", 16, 16, 1024, 64, False, "normal", 1),
+    Workload("n4096_d128", 16, 16, 4096, 128, False, "normal", 2),
+    Workload("n8192_d128_c", 8, 16, 8192, 128, True, "normal", 3),
+    Workload("n16384_d128_c", 4, 32, 16384, 128, True, "peaky_t3", 4),
+)
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _student_t3(g: torch.Generator, shape) -> torch.Tensor:
+    z = torch.randn(shape, generator=g, dtype=torch.float32)
+    w = torch.randn(tuple(shape) + (3,), generator=g, dtype=torch.float32)
+    chi2_over_nu = (w * w).sum(dim=-1) / 3.0
+    return z / torch.sqrt(chi2_over_nu)
+
+
+def draw(shape, seed: int, dist: str = "normal"):
+    """Q, K, V as bf16 CPU tensors of `shape`, per the recipe above."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    if dist == "normal":
+        q = torch.randn(shape, generator=g, dtype=torch.float32)
+        k = torch.randn(shape, generator=g, dtype=torch.float32)
+        v = torch.randn(shape, generator=g, dtype=torch.float32)
+    elif dist == "peaky_t3":
+        q = 4.0 * torch.randn(shape, generator=g, dtype=torch.float32)
+        k = 4.0 * torch.randn(shape, generator=g, dtype=torch.float32)
+        v = _student_t3(g, shape).clamp_(-8.0, 8.0)
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
+
+
+def workload_inputs(w: Workload):
+    return draw(w.shape, w.seed, w.dist)

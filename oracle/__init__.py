@@ -1,0 +1,35 @@
+"""fp64 CPU oracle for the fused attention forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import, call or build anything in this
+package.  The CUDA library never links or loads it, and the two share no code:
+this package computes attention from its plain definition, in double
+precision, so the GPU kernels have something independent to be checked against.
+
+Contents
+  attention_rows   plain definition (C, OpenMP, fp64) for chosen rows
+  attention        the same for every row of a [B, H, N, D] problem
+  tiled_online_softmax
+                   numpy restatement of the tile-by-tile online-softmax
+                   recurrence the kernel examples on the pages use, both in
+                   the pages' per-step-renormalising form and in the
+                   deferred-division form; tiny sizes only.
+  build            compile the C part (called by the graft entry's build()).
+
+Sources: the attention definition computed by the "RTX 4090 flash attention"
+and "H100 FlashAttention-2 forward" examples in the ThunderKittens news
+write-up (88811315.cn, post 77732); the causal mask and the log-sum-exp follow
+the plainest reading of the requested interface (keys j <= i visible; natural
+log over scaled, masked scores).
+"""
+from .brute import attention, attention_rows, build, lib_path, max_threads
+from .tiled import tiled_online_softmax
+
+__all__ = [
+    "attention",
+    "attention_rows",
+    "build",
+    "lib_path",
+    "max_threads",
+    "tiled_online_softmax",
+]

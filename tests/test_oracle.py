@@ -1,0 +1,230 @@
+"""Pins for the fp64 oracle: closed forms, invariants, special cases.
+
+Each test fixes a property that the definition O = softmax(scale Q K^T
+[+ causal mask]) V, LSE = ln sum exp(scores) forces, chosen so that a plausible
+slip in the oracle (a dropped term, a wrong sign or index, a transposed
+operand, log base 2 instead of e, an off-by-one causal mask) fails at least
+one of them.  No GPU needed.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from attention_forward_tk_gb300.inputs import draw
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")
+
+
+def bits(x):
+    """float array of bf16-exact values -> bf16 bit patterns (uint16)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    assert torch.equal(t.float(), torch.as_tensor(np.asarray(x, dtype=np.float32))), \
+        "test inputs must be exact in bf16"
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def widen(t):
+    return t.double().numpy()
+
+
+def run(oracle_lib, q, k, v, scale, causal, **kw):
+    return oracle_lib.attention(q, k, v, scale, causal, **kw)
+
+
+# --------------------------------------------------------------------------
+# hand-derived golden cases
+
+
+def test_golden_closed_forms(oracle_lib):
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    assert len(cases) >= 4
+    for c in cases:
+        o, lse = run(oracle_lib, bits(c["q"]), bits(c["k"]), bits(c["v"]),
+                     c["scale"], c["causal"])
+        np.testing.assert_allclose(o, np.asarray(c["o"], float), rtol=0, atol=1e-12,
+                                   err_msg=c["name"])
+        np.testing.assert_allclose(lse, np.asarray(c["lse"], float), rtol=0,
+                                   atol=1e-12, err_msg=c["name"])
+
+
+# --------------------------------------------------------------------------
+# invariants and closed forms on random bf16 inputs
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_of_p_sum_to_one(oracle_lib, causal):
+    # V = 1 makes O_i = sum_j P_ij exactly.
+    q, k, _ = draw((2, 3, 37, 16), seed=11)
+    v = torch.ones_like(q)
+    o, _ = run(oracle_lib, q, k, v, 0.25, causal)
+    np.testing.assert_allclose(o, 1.0, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_gives_constant_o(oracle_lib, causal):
+    q, k, v = draw((1, 2, 29, 8), seed=12)
+    row = v[0, 0, 0].clone()
+    vc = row.expand_as(v).contiguous()
+    o, _ = run(oracle_lib, q, k, vc, 0.3, causal)
+    np.testing.assert_allclose(o, np.broadcast_to(widen(row), o.shape), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_shift_moves_lse_only(oracle_lib, causal):
+    q, k, v = draw((1, 1, 40, 16), seed=13)
+    rows = np.arange(40)
+    shifts = np.linspace(-7.0, 11.0, 40)
+    o0, l0, _ = oracle_lib.attention_rows(q, k, v, 0.25, causal, rows)
+    o1, l1, _ = oracle_lib.attention_rows(q, k, v, 0.25, causal, rows, shifts)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1 - l0, shifts, rtol=0, atol=1e-12)
+
+
+def test_single_key(oracle_lib):
+    q, k, v = draw((2, 2, 1, 64), seed=14)
+    o, lse = run(oracle_lib, q, k, v, 0.125, False)
+    np.testing.assert_array_equal(o, widen(v))
+    dot = (widen(q) * widen(k)).sum(-1)
+    np.testing.assert_allclose(lse, 0.125 * dot, rtol=0, atol=1e-12)
+
+
+def test_causal_row_zero_is_v0(oracle_lib):
+    q, k, v = draw((1, 3, 50, 32), seed=15)
+    o, lse = run(oracle_lib, q, k, v, 0.2, True)
+    np.testing.assert_array_equal(o[:, :, 0, :], widen(v)[:, :, 0, :])
+    dot = (widen(q)[:, :, 0] * widen(k)[:, :, 0]).sum(-1)
+    np.testing.assert_allclose(lse[:, :, 0], 0.2 * dot, rtol=0, atol=1e-12)
+
+
+def test_zero_query_is_uniform(oracle_lib):
+    _, k, v = draw((1, 2, 33, 16), seed=16)
+    q = torch.zeros_like(k)
+    n = 33
+    o, lse = run(oracle_lib, q, k, v, 0.5, False)
+    np.testing.assert_allclose(o, np.broadcast_to(widen(v).mean(axis=2, keepdims=True), o.shape),
+                               rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, math.log(n), rtol=0, atol=1e-12)
+    o, lse = run(oracle_lib, q, k, v, 0.5, True)
+    prefix_mean = np.cumsum(widen(v), axis=2) / np.arange(1, n + 1)[None, None, :, None]
+    np.testing.assert_allclose(o, prefix_mean, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.log(np.arange(1, n + 1))[None, None, :].repeat(2, 1),
+                               rtol=0, atol=1e-12)
+
+
+def test_two_keys_sigmoid(oracle_lib):
+    q, k, v = draw((1, 1, 2, 16), seed=17)
+    qd, kd, vd = widen(q)[0, 0], widen(k)[0, 0], widen(v)[0, 0]
+    scale = 0.37
+    o, lse = run(oracle_lib, q, k, v, scale, False)
+    for i in range(2):
+        s0, s1 = scale * qd[i] @ kd[0], scale * qd[i] @ kd[1]
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+        np.testing.assert_allclose(o[0, 0, i], w0 * vd[0] + w1 * vd[1], rtol=0, atol=1e-12)
+        hi = max(s0, s1)
+        np.testing.assert_allclose(lse[0, 0, i], hi + math.log1p(math.exp(min(s0, s1) - hi)),
+                                   rtol=0, atol=1e-12)
+
+
+def test_permuting_kv_rows_together(oracle_lib):
+    q, k, v = draw((1, 2, 45, 16), seed=18)
+    perm = torch.randperm(45, generator=torch.Generator().manual_seed(5))
+    o0, l0 = run(oracle_lib, q, k, v, 0.25, False)
+    o1, l1 = run(oracle_lib, q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(),
+                 0.25, False)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l0, rtol=0, atol=1e-12)
+    # permuting K alone must change the result (V rows no longer match K rows)
+    o2, _ = run(oracle_lib, q, k[:, :, perm].contiguous(), v, 0.25, False)
+    assert np.abs(o2 - o0).max() > 1e-3
+    # permuting Q rows permutes the outputs
+    o3, l3 = run(oracle_lib, q[:, :, perm].contiguous(), k, v, 0.25, False)
+    np.testing.assert_allclose(o3, o0[:, :, perm.numpy()], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l3, l0[:, :, perm.numpy()], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_v_power_of_two_homogeneity(oracle_lib, causal):
+    q, k, v = draw((1, 1, 31, 8), seed=19)
+    o0, _ = run(oracle_lib, q, k, v, 0.3, causal)
+    o1, _ = run(oracle_lib, q, k, (v.float() * 8).to(torch.bfloat16), 0.3, causal)
+    np.testing.assert_array_equal(o1, 8 * o0)
+
+
+def test_causal_row_equals_full_prefix(oracle_lib):
+    q, k, v = draw((1, 1, 24, 16), seed=20)
+    oc, lc = run(oracle_lib, q, k, v, 0.25, True)
+    for i in (0, 1, 7, 23):
+        qs = q[:, :, : i + 1].contiguous()
+        ks = k[:, :, : i + 1].contiguous()
+        vs = v[:, :, : i + 1].contiguous()
+        of, lf = run(oracle_lib, qs, ks, vs, 0.25, False)
+        np.testing.assert_allclose(oc[0, 0, i], of[0, 0, i], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lc[0, 0, i], lf[0, 0, i], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_lse_bounds(oracle_lib, causal):
+    q, k, v = draw((1, 1, 64, 32), seed=21, dist="peaky_t3")
+    scale = 1 / math.sqrt(32)
+    _, lse = run(oracle_lib, q, k, v, scale, causal)
+    s = scale * widen(q)[0, 0] @ widen(k)[0, 0].T
+    n = 64
+    for i in range(n):
+        vis = s[i, : i + 1] if causal else s[i]
+        assert vis.max() - 1e-12 <= lse[0, 0, i] <= vis.max() + math.log(vis.size) + 1e-12
+
+
+# --------------------------------------------------------------------------
+# second routines: tiled online softmax and the library's attention
+
+
+@pytest.mark.parametrize("mode", ["deferred", "renormalize"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_brute_force_matches_tiled_online_softmax(oracle_lib, mode, causal):
+    from oracle import tiled_online_softmax
+    for n, bq, bk in [(1, 1, 1), (5, 2, 3), (17, 4, 5), (33, 16, 16), (64, 7, 9), (64, 64, 16)]:
+        q, k, v = draw((1, 1, n, 16), seed=100 + n, dist="peaky_t3")
+        scale = 0.25
+        o, lse = run(oracle_lib, q, k, v, scale, causal)
+        ot, lt = tiled_online_softmax(widen(q)[0, 0], widen(k)[0, 0], widen(v)[0, 0],
+                                      scale, causal, bq, bk, mode)
+        np.testing.assert_allclose(ot, o[0, 0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lt, lse[0, 0], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_torch_sdpa_float64(oracle_lib, causal):
+    q, k, v = draw((2, 2, 70, 64), seed=22)
+    scale = 0.125
+    o, lse = run(oracle_lib, q, k, v, scale, causal)
+    qd, kd, vd = q.double(), k.double(), v.double()
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, is_causal=causal,
+                                                           scale=scale)
+    s = scale * qd @ kd.transpose(-1, -2)
+    if causal:
+        s = s.masked_fill(torch.ones(70, 70, dtype=torch.bool).triu(1), float("-inf"))
+    ref_lse = torch.logsumexp(s, dim=-1)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_row_subset_matches_full(oracle_lib):
+    q, k, v = draw((2, 3, 20, 16), seed=23)
+    o, lse = run(oracle_lib, q, k, v, 0.25, True)
+    rows = np.array([0, 19, 20, 59, 119, 77])
+    os_, ls, used = oracle_lib.attention_rows(q, k, v, 0.25, True, rows)
+    assert used >= 1
+    np.testing.assert_array_equal(os_, o.reshape(-1, 16)[rows])
+    np.testing.assert_array_equal(ls, lse.reshape(-1)[rows])
+
+
+def test_rejects_bad_rows(oracle_lib):
+    q, k, v = draw((1, 1, 4, 8), seed=24)
+    with pytest.raises(ValueError):
+        oracle_lib.attention_rows(q, k, v, 0.25, False, [4])
