@@ -1,0 +1,22 @@
+"""GB300-native fused attention forward.
+
+O = softmax(scale * Q K^T [+ causal mask]) V with the per-row log-sum-exp, on
+bf16 [B, H, N, D] tensors, computed by hand-written sm_103a CUDA kernels behind
+a C ABI (``include/tk_attn.h``).  This package is the thin Python binding over
+that library: argument marshalling only.  The shared library is loaded on first
+use; if it is missing or cannot be loaded, every call raises.
+"""
+from .api import (  # noqa: F401
+    TkAttnError,
+    attention_forward,
+    attention_forward_host,
+    last_device_error,
+    library,
+    status_string,
+    tk_attn_check_args,
+    tk_attn_fwd,
+    tk_attn_last_device_error,
+    tk_attn_status_string,
+    tk_attn_version,
+    version,
+)

@@ -1,0 +1,191 @@
+"""ctypes binding over the C ABI declared in ``include/tk_attn.h``.
+
+Argument marshalling only: every step of the attention forward pass runs in
+the CUDA kernels of ``libtk_attn.so``.  PyTorch supplies device memory and
+streams.  The library is built in-tree (``attention_forward_tk_gb300/_build``)
+by :func:`attention_forward_tk_gb300.build.build_library`; if it is missing or
+fails to load, every call raises :class:`TkAttnError` -- there is no fallback.
+
+The functions named ``tk_attn_*`` mirror the C entry points one for one and
+take raw integers (device addresses, sizes, a stream handle).  The
+``attention_forward*`` helpers wrap them for torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtk_attn.so")
+
+TK_ATTN_OK = 0
+TK_ATTN_ERR_INVALID_ARG = -1
+TK_ATTN_ERR_UNSUPPORTED = -2
+TK_ATTN_ERR_ARCH = -3
+TK_ATTN_ERR_LAUNCH = -4
+TK_ATTN_ERR_DEVICE_TIMEOUT = -5
+
+# every symbol include/tk_attn.h declares
+EXPORTED = (
+    "tk_attn_fwd",
+    "tk_attn_check_args",
+    "tk_attn_status_string",
+    "tk_attn_version",
+    "tk_attn_last_device_error",
+)
+
+
+class TkAttnError(RuntimeError):
+    """A non-zero status from the library, or the library could not be loaded."""
+
+    def __init__(self, msg: str, status: int | None = None):
+        super().__init__(msg)
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Load libtk_attn.so once and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise TkAttnError(
+                f"{LIB_PATH} is missing: build it with "
+                "attention_forward_tk_gb300.build.build_library()")
+        try:
+            lib = ctypes.CDLL(LIB_PATH)
+        except OSError as e:  # pragma: no cover - depends on the machine
+            raise TkAttnError(f"cannot load {LIB_PATH}: {e}") from e
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.tk_attn_fwd.restype = i
+        lib.tk_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.tk_attn_check_args.restype = i
+        lib.tk_attn_check_args.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i]
+        lib.tk_attn_status_string.restype = ctypes.c_char_p
+        lib.tk_attn_status_string.argtypes = [i]
+        lib.tk_attn_version.restype = i
+        lib.tk_attn_version.argtypes = []
+        lib.tk_attn_last_device_error.restype = i
+        lib.tk_attn_last_device_error.argtypes = [vp]
+        _lib = lib
+        return _lib
+
+
+# ----------------------------------------------------------------- raw C calls
+
+
+def tk_attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int,
+                D: int, scale: float, causal: int, stream: int) -> int:
+    return int(library().tk_attn_fwd(q, k, v, o, lse, B, H, N, D, ctypes.c_float(scale),
+                                     int(causal), stream))
+
+
+def tk_attn_check_args(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int,
+                       D: int, scale: float, causal: int) -> int:
+    return int(library().tk_attn_check_args(q, k, v, o, lse, B, H, N, D,
+                                            ctypes.c_float(scale), int(causal)))
+
+
+def tk_attn_status_string(status: int) -> str:
+    return library().tk_attn_status_string(int(status)).decode()
+
+
+def tk_attn_version() -> int:
+    return int(library().tk_attn_version())
+
+
+def tk_attn_last_device_error(stream: int) -> int:
+    return int(library().tk_attn_last_device_error(stream))
+
+
+# short aliases
+status_string = tk_attn_status_string
+version = tk_attn_version
+
+
+def last_device_error(stream=None) -> int:
+    return tk_attn_last_device_error(_stream_handle(stream))
+
+
+# ----------------------------------------------------------------- torch helpers
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int):
+    if status != TK_ATTN_OK:
+        raise TkAttnError(f"tk_attn_fwd: {tk_attn_status_string(status)} ({status})", status)
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
+                      out=None, lse=None, stream=None):
+    """O, LSE = attention forward of bf16 CUDA tensors [B, H, N, D].
+
+    Enqueued on `stream` (default: torch's current stream); returns
+    immediately.  `out` (bf16 [B,H,N,D]) and `lse` (fp32 [B,H,N]) are
+    allocated by torch when not given.
+    """
+    import torch
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must be [B, H, N, D] tensors of one shape")
+    B, H, N, D = (int(x) for x in q.shape)
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(tk_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       lse.data_ptr(), B, H, N, D, float(scale), int(bool(causal)),
+                       _stream_handle(stream)))
+    return out, lse
+
+
+def attention_forward_host(q, k, v, causal: bool = False, scale: float | None = None,
+                           device_buffers=None, out=None, lse=None, stream=None):
+    """The same call for bf16 tensors in (preferably pinned) host memory.
+
+    Copies q, k, v to the device, runs tk_attn_fwd, copies O and LSE back into
+    host tensors `out` / `lse` (allocated pinned when not given) and waits for
+    the stream.  `device_buffers` = (q_d, k_d, v_d, o_d, lse_d) reuses device
+    memory between calls.  Returns (out, lse) on the host.
+    """
+    import torch
+    B, H, N, D = (int(x) for x in q.shape)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if device_buffers is None:
+        device_buffers = (torch.empty_like(q, device=dev), torch.empty_like(k, device=dev),
+                          torch.empty_like(v, device=dev), torch.empty_like(q, device=dev),
+                          torch.empty((B, H, N), dtype=torch.float32, device=dev))
+    qd, kd, vd, od, ld = device_buffers
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        qd.copy_(q, non_blocking=True)
+        kd.copy_(k, non_blocking=True)
+        vd.copy_(v, non_blocking=True)
+        attention_forward(qd, kd, vd, causal, scale, out=od, lse=ld, stream=s)
+        out.copy_(od, non_blocking=True)
+        lse.copy_(ld, non_blocking=True)
+    s.synchronize()
+    return out, lse

@@ -1,0 +1,230 @@
+// tk_attn.cu -- host side of the attention forward library: argument checks,
+// TMA tensor-map encoding, persistent-grid sizing and the C ABI declared in
+// include/tk_attn.h.  The device work is in tk_attn_fwd.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <mutex>
+
+#include "tk_attn.h"
+#include "tk_attn_fwd.cuh"
+
+namespace tkattn {
+namespace {
+
+// Device error word: kernels record a bounded wait that ran out here.
+__device__ int g_dev_error;
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  std::once_flag once;
+  int status = TK_ATTN_ERR_ARCH;
+  int num_sms = 0;
+  int *err_word = nullptr;  // address of g_dev_error on this device
+};
+
+DeviceState g_dev[kMaxDevices];
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+template <int D, bool kCausal>
+int configure_kernel() {
+  auto kern = tk_attn_fwd_kernel<D, kCausal>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           FwdCfg<D>::kSmemAlloc) != cudaSuccess)
+    return TK_ATTN_ERR_LAUNCH;
+  // The register split between warpgroups (setmaxnreg) assumes the kernel is
+  // launched with exactly 128 registers per thread; refuse anything else.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TK_ATTN_ERR_LAUNCH;
+  if (fa.numRegs != 128) return TK_ATTN_ERR_LAUNCH;
+  return TK_ATTN_OK;
+}
+
+// Per-device set-up, once, with that device current.
+void init_device(int dev, DeviceState &ds) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ds.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    ds.status = TK_ATTN_ERR_ARCH;
+    return;
+  }
+  if (major != 10 || minor != 3) {  // the kernels are built for sm_103a only
+    ds.status = TK_ATTN_ERR_ARCH;
+    return;
+  }
+  int st = configure_kernel<64, false>();
+  if (!st) st = configure_kernel<64, true>();
+  if (!st) st = configure_kernel<128, false>();
+  if (!st) st = configure_kernel<128, true>();
+  if (!st && cudaGetSymbolAddress(reinterpret_cast<void **>(&ds.err_word), g_dev_error) !=
+                 cudaSuccess)
+    st = TK_ATTN_ERR_LAUNCH;
+  if (!st && cudaMemset(ds.err_word, 0, sizeof(int)) != cudaSuccess) st = TK_ATTN_ERR_LAUNCH;
+  if (!st && cudaDeviceSynchronize() != cudaSuccess) st = TK_ATTN_ERR_LAUNCH;
+  ds.status = st;
+}
+
+DeviceState *current_device(int *status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *status = TK_ATTN_ERR_ARCH;
+    return nullptr;
+  }
+  DeviceState &ds = g_dev[dev];
+  std::call_once(ds.once, init_device, dev, std::ref(ds));
+  *status = ds.status;
+  return ds.status == TK_ATTN_OK ? &ds : nullptr;
+}
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// [BH, N, D] bf16 viewed as a 3-D tensor (d fastest); boxes of 64 columns x
+// 128 rows x 1 slice with the 128-byte swizzle the MMA descriptors expect.
+// Rows past N read as zero, which is what ragged tiles need.
+bool make_map(CUtensorMap *map, const void *ptr, int BH, int N, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
+  return a < b + nb && b < a + na;
+}
+
+template <int D, bool kCausal>
+cudaError_t launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                   const FwdParams &p, int grid, cudaStream_t stream) {
+  tk_attn_fwd_kernel<D, kCausal>
+      <<<grid, FwdCfg<D>::kThreads, FwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace tkattn
+
+using namespace tkattn;
+
+extern "C" int tk_attn_check_args(const void *q, const void *k, const void *v, const void *o,
+                                  const float *lse, int B, int H, int N, int D, float scale,
+                                  int causal) {
+  (void)causal;
+  if (!q || !k || !v || !o || !lse) return TK_ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return TK_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TK_ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return TK_ATTN_ERR_UNSUPPORTED;
+  const uintptr_t pq = (uintptr_t)q, pk = (uintptr_t)k, pv = (uintptr_t)v, po = (uintptr_t)o,
+                  pl = (uintptr_t)lse;
+  if ((pq | pk | pv | po | pl) & 15u) return TK_ATTN_ERR_UNSUPPORTED;
+  // sizes: B*H slices and the unit count must fit an int; tensor bytes must
+  // fit the tensor map's 40-bit stride range.
+  const long long BH = (long long)B * H;
+  const long long units = BH * ((N + 255LL) / 256);
+  if (BH > 0x7fffffffLL || units > 0x7fffffffLL) return TK_ATTN_ERR_UNSUPPORTED;
+  const unsigned long long elems = (unsigned long long)BH * (unsigned long long)N * D;
+  const unsigned long long tensor_bytes = elems * 2ull;
+  if (tensor_bytes >= (1ull << 40)) return TK_ATTN_ERR_UNSUPPORTED;
+  const size_t lse_bytes = (size_t)BH * (size_t)N * 4u;
+  // outputs must not overlap each other or any input
+  if (overlaps(po, tensor_bytes, pl, lse_bytes)) return TK_ATTN_ERR_INVALID_ARG;
+  const uintptr_t ins[3] = {pq, pk, pv};
+  for (uintptr_t in : ins)
+    if (overlaps(po, tensor_bytes, in, tensor_bytes) || overlaps(pl, lse_bytes, in, tensor_bytes))
+      return TK_ATTN_ERR_INVALID_ARG;
+  return TK_ATTN_OK;
+}
+
+extern "C" int tk_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int B, int H, int N, int D, float scale, int causal,
+                           tk_attn_stream_t stream) {
+  int st = tk_attn_check_args(q, k, v, o, lse, B, H, N, D, scale, causal);
+  if (st) return st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, BH, N, D) || !make_map(&tk, k, BH, N, D) || !make_map(&tv, v, BH, N, D))
+    return TK_ATTN_ERR_LAUNCH;
+  FwdParams p;
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.err = ds->err_word;
+  p.BH = BH;
+  p.N = N;
+  p.num_mblocks = (N + 255) / 256;
+  p.num_units = BH * p.num_mblocks;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (D == 64)
+    e = causal ? launch<64, true>(tq, tk, tv, p, grid, s) : launch<64, false>(tq, tk, tv, p, grid, s);
+  else
+    e = causal ? launch<128, true>(tq, tk, tv, p, grid, s)
+               : launch<128, false>(tq, tk, tv, p, grid, s);
+  return e == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
+}
+
+extern "C" const char *tk_attn_status_string(int status) {
+  switch (status) {
+    case TK_ATTN_OK: return "ok";
+    case TK_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case TK_ATTN_ERR_UNSUPPORTED: return "unsupported head dim, alignment or size";
+    case TK_ATTN_ERR_ARCH: return "no compute-capability 10.3 GPU current";
+    case TK_ATTN_ERR_LAUNCH: return "CUDA error while preparing or launching the kernel";
+    case TK_ATTN_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a barrier wait";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int tk_attn_version(void) { return TK_ATTN_VERSION; }
+
+extern "C" int tk_attn_last_device_error(tk_attn_stream_t stream) {
+  int st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, ds->err_word, sizeof(int), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return TK_ATTN_ERR_LAUNCH;
+  }
+  if (word != 0) {
+    if (cudaMemsetAsync(ds->err_word, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return TK_ATTN_ERR_LAUNCH;
+    return TK_ATTN_ERR_DEVICE_TIMEOUT;
+  }
+  return TK_ATTN_OK;
+}

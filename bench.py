@@ -1,0 +1,413 @@
+"""Benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tk|reference]
+                    [--workload NAME] [--all-workloads]
+
+One step = one tk_attn_fwd call (the whole hot path: TMA loads, QK^T,
+online softmax, PV, epilogue) over one batch of synthetic inputs resident in
+HBM.  The default workload is B16 H16 N1024 D64 non-causal; the metric is
+TFLOP/s with F = 4*B*H*N^2*D (halved under the causal mask) and its fraction
+of the measured dense bf16 tensor peak.  L2 (126 MB) is flushed by writing a
+256 MB buffer before every timed step; each step is timed with CUDA events on
+the launching stream.  Rank 0 prints one JSON line.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas: the path has no exchange step); `value` is the work of all ranks
+divided by the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of rows of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "n1024_d64"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ("attention_forward_tk_gb300/csrc/tk_attn_fwd.cuh",
+                  "attention_forward_tk_gb300/csrc/sm103_ptx.cuh",
+                  "attention_forward_tk_gb300/csrc/tk_attn.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_NAME = "tk_attn_fwd_kernel"
+
+
+# ---------------------------------------------------------------- helpers
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    src = kernel_source_hash()
+    for line in open(TRAFFIC_FILE):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload \
+                and parts[1] == src:
+            return float(parts[2])
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+
+def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on random rows of the workload for about
+    `budget_s` seconds.  Returns (TFLOP/s, threads, rows, seconds)."""
+    import numpy as np
+
+    import oracle
+    from attention_forward_tk_gb300.inputs import workload_inputs
+
+    oracle.build()
+    q, k, v = workload_inputs(w)  # the recipe's CPU values
+    BH = w.B * w.H
+    rng = np.random.default_rng(seed)
+
+    def row_flops(rows):
+        i = rows % w.N
+        keys = (i + 1) if w.causal else np.full_like(i, w.N)
+        return float((4.0 * w.D * keys).sum())
+
+    # calibrate on a small batch, then run one batch sized to the budget
+    rows = rng.integers(0, BH * w.N, size=64)
+    t0 = time.perf_counter()
+    _, _, threads = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(min(BH * w.N, max(64, 64 * budget_s / dt)))
+    rows = rng.integers(0, BH * w.N, size=n)
+    t0 = time.perf_counter()
+    _, _, threads = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    dt = time.perf_counter() - t0
+    return row_flops(rows) / dt / 1e12, threads, n, dt
+
+
+# ---------------------------------------------------------------- GPU leg
+
+
+def time_gpu(w, steps: int, warmup: int, device):
+    """CUDA-event time of `steps` tk_attn_fwd launches (L2 flushed before each)."""
+    import torch
+
+    from attention_forward_tk_gb300 import api
+    from attention_forward_tk_gb300.inputs import workload_inputs
+
+    q, k, v = workload_inputs(w, device=device)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            w.B, w.H, w.N, w.D, w.scale, int(w.causal), sh)
+    for _ in range(warmup):
+        flush.zero_()
+        st = api.tk_attn_fwd(*args)
+        if st:
+            raise RuntimeError(api.tk_attn_status_string(st))
+    if api.tk_attn_last_device_error(sh) != 0:
+        raise RuntimeError("device-side barrier timeout during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        api.tk_attn_fwd(*args)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    if api.tk_attn_last_device_error(sh) != 0:
+        raise RuntimeError("device-side barrier timeout during timing")
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return ms, wall, steps
+
+
+def time_e2e(w, steps: int, warmup: int, device):
+    """The same call from pinned host buffers: H2D of Q, K, V, the kernel, and
+    D2H of O and LSE every step, timed with CUDA events around all of it."""
+    import torch
+
+    from attention_forward_tk_gb300 import attention_forward_host
+    from attention_forward_tk_gb300.inputs import workload_inputs
+
+    q, k, v = (t.cpu().pin_memory() for t in workload_inputs(w, device=device))
+    bufs = (torch.empty_like(q, device=device), torch.empty_like(k, device=device),
+            torch.empty_like(v, device=device), torch.empty_like(q, device=device),
+            torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device))
+    o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, pin_memory=True)
+    for _ in range(warmup):
+        attention_forward_host(q, k, v, w.causal, w.scale, bufs, o, lse)
+    stream = torch.cuda.current_stream(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    a.record(stream)
+    for _ in range(steps):
+        attention_forward_host(q, k, v, w.causal, w.scale, bufs, o, lse)
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    h2d = 3 * q.numel() * 2
+    d2h = o.numel() * 2 + lse.numel() * 4
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("tk", "reference"), default="tk")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="also time every other measured workload (extra key)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="budget of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer leg (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from attention_forward_tk_gb300.inputs import BY_NAME, WORKLOADS
+    w = BY_NAME[args.workload]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        return main_reference(args, w, world, rank)
+
+    import torch
+    import torch.distributed as dist
+
+    from attention_forward_tk_gb300.build import build_library
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    if rank == 0:
+        build_library()
+    if world > 1:
+        dist.barrier()
+    from attention_forward_tk_gb300 import api
+    api.library()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    barrier()
+    with ClockSampler(device.index if world == 1 else local) as clk:
+        barrier()
+        ms, wall, launches = time_gpu(w, args.steps, args.warmup, device)
+        barrier()
+    kernel_ms = statistics.mean(ms)
+    t_total = sum(ms) / 1e3
+    if world > 1:
+        t = torch.tensor([t_total, wall], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_total, wall = float(t[0]), float(t[1])
+    value = world * w.flops * args.steps / t_total / 1e12
+
+    e2e_ms, h2d, d2h = (time_e2e(w, max(3, args.steps // 5), 3, device)
+                        if not args.no_e2e else (float("nan"), 0, 0))
+    e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
+    if world > 1 and not args.no_e2e:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_value = world * w.flops / (float(t[0]) / 1e3) / 1e12
+
+    extra = {}
+    if args.all_workloads:
+        for ow in WORKLOADS:
+            oms, _, _ = time_gpu(ow, max(5, args.steps // 5), 3, device)
+            m = statistics.median(oms)
+            extra[ow.name] = {"ms": round(m, 4), "tflops": round(ow.flops / m / 1e9, 1)}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peak_tf, peak_hbm, peak_kind = measured_peaks()
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": "attention fwd TFLOP/s (bf16, 1xGB300) and % of dense BF16 tensor peak",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_total * 1e3 / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "causal": w.causal, "values": w.dist, "flops_per_step": w.flops,
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4),
+                     "peak_kind": f"{peak_kind} dense bf16 (burst)",
+                     "traffic": traffic,
+                     "algorithmic_bytes": w.io_bytes,
+                     "hbm_gbs": round(w.io_bytes / (kernel_ms / 1e3) / 1e9, 1),
+                     "hbm_peak_gbs": peak_hbm},
+        "e2e": None if args.no_e2e else {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches,
+        "wall_s_timed_region": round(wall, 4),
+        "kernel_ms_median": round(statistics.median(ms), 5),
+        "clocks": clk.summary(),
+    }
+    if extra:
+        line["all_workloads"] = extra
+    if not args.no_cpu_baseline and world >= 1:
+        tf, threads, n, dt = cpu_oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{n} random rows of {w.name}, fp64, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main_reference(args, w, world, rank):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    samples = []
+    threads = 0
+    per_step = max(1.0, min(20.0, 150.0 / (args.steps + args.warmup)))
+    for i in range(args.warmup):
+        cpu_oracle_sample(w, per_step, seed=1000 + i)
+    for i in range(args.steps):
+        tf, threads, n, dt = cpu_oracle_sample(w, per_step, seed=i)
+        samples.append((tf, n, dt))
+    value = statistics.mean(s[0] for s in samples)
+    ms = statistics.mean(w.flops / (s[0] * 1e12) * 1e3 for s in samples)
+    line = {
+        "impl": "reference",
+        "metric": "attention fwd TFLOP/s (bf16, 1xGB300) and % of dense BF16 tensor peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "causal": w.causal, "values": w.dist, "flops_per_step": w.flops},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{samples[0][1]} random rows of {w.name} per step "
+                                   f"(~{per_step:.0f} s of fp64 work)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,112 @@
+/*
+ * tk_attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The operation (one call = one whole forward pass over B*H independent
+ * (batch, head) slices):
+ *
+ *   O[b,h]   = softmax( scale * Q[b,h] K[b,h]^T  [+ causal mask] ) V[b,h]
+ *   LSE[b,h,i] = ln sum_j exp( scale * q_i . k_j )   over the visible keys j
+ *
+ * This is the attention that the flash-attention kernel examples compute in
+ * the ThunderKittens news write-up (88811315.cn, post 77732): the "RTX 4090
+ * flash attention" example (head dim 64) and the "H100 FlashAttention-2
+ * forward" example (head dims 64 and 128), which stream K/V in tiles with an
+ * online softmax so the N x N score matrix never reaches memory.  Those
+ * examples fold a fixed scale (0.125 = 1/sqrt(64), 0.08838834764 = 1/sqrt(128))
+ * into Q; here the scale is an argument, applied in fp32 to the fp32 scores.
+ * The causal mask (key j visible to query i iff j <= i, diagonal included)
+ * and the LSE output are not in those examples; they follow the plainest
+ * reading of this interface (natural log, over the scaled, masked scores).
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major, in GPU device memory owned by the caller:
+ *       q, k, v, o : bf16  [B, H, N, D]   (element (b,h,i,d) at ((b*H+h)*N+i)*D+d)
+ *       lse        : fp32  [B, H, N]
+ *     Base addresses must be 16-byte aligned.  o and lse must not overlap each
+ *     other or any input.
+ *   - The library allocates no device memory, never frees caller memory and
+ *     never synchronises the stream (except tk_attn_last_device_error).  Work
+ *     is enqueued on `stream` (0 = the legacy default stream) and runs
+ *     asynchronously; results are valid once the stream reaches that point.
+ *   - Return value: TK_ATTN_OK (0) or a negative TK_ATTN_ERR_* code.  On any
+ *     error no work is enqueued and the outputs are left untouched.
+ *   - Thread safety: calls may come from several host threads; cached host
+ *     state (device properties, the driver entry point) is initialised once.
+ *
+ * `tk_attn_stream_t` is the CUDA runtime's stream handle type (cudaStream_t),
+ * declared here without CUDA headers so plain C callers can include this file.
+ */
+#ifndef TK_ATTN_H_
+#define TK_ATTN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *tk_attn_stream_t;
+
+#define TK_ATTN_OK 0
+#define TK_ATTN_ERR_INVALID_ARG (-1)   /* null pointer, B/H/N <= 0, bad scale, overlap */
+#define TK_ATTN_ERR_UNSUPPORTED (-2)   /* D not 64 or 128, pointer not 16-byte aligned,
+                                          or sizes beyond the 32-bit tensor-map ranges */
+#define TK_ATTN_ERR_ARCH (-3)          /* current device is not a compute-capability
+                                          10.3 (sm_103a) GPU, or no device */
+#define TK_ATTN_ERR_LAUNCH (-4)        /* CUDA reported an error building tensor maps
+                                          or launching the kernel */
+#define TK_ATTN_ERR_DEVICE_TIMEOUT (-5) /* a kernel gave up waiting on an on-chip
+                                           barrier (reported by
+                                           tk_attn_last_device_error only) */
+
+#define TK_ATTN_VERSION 10000 /* major*10000 + minor*100 + patch */
+
+/*
+ * tk_attn_fwd -- fused attention forward, asynchronous on `stream`.
+ *
+ *   q, k, v  [in]  device bf16 [B,H,N,D]
+ *   o        [out] device bf16 [B,H,N,D]; o = bf16_rne(softmax(...) V)
+ *   lse      [out] device fp32 [B,H,N]; natural-log log-sum-exp of the scaled,
+ *                  masked scores of each row
+ *   B, H, N  >= 1; any N (no multiple-of-tile requirement)
+ *   D        64 or 128
+ *   scale    finite and > 0 (usually 1/sqrt(D))
+ *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i
+ *   stream   CUDA stream to enqueue on
+ *
+ * Limits: B*H*N*D must stay below 2^31 elements per tensor map dimension
+ * product (checked), N < 2^31.
+ * Errors: TK_ATTN_ERR_INVALID_ARG, _UNSUPPORTED, _ARCH, _LAUNCH (see above).
+ */
+int tk_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                int B, int H, int N, int D, float scale, int causal,
+                tk_attn_stream_t stream);
+
+/*
+ * tk_attn_check_args -- the host-side argument validation of tk_attn_fwd,
+ * without touching the GPU.  Same arguments (minus the stream); returns the
+ * code tk_attn_fwd would return before any CUDA call (TK_ATTN_OK,
+ * _INVALID_ARG or _UNSUPPORTED).  Pointers are only compared, never read.
+ */
+int tk_attn_check_args(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, int B, int H, int N, int D, float scale,
+                       int causal);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char *tk_attn_status_string(int status);
+
+/* TK_ATTN_VERSION of the loaded library. */
+int tk_attn_version(void);
+
+/*
+ * tk_attn_last_device_error -- synchronises `stream`, then returns and clears
+ * the device-side error word of the current device: TK_ATTN_OK, or
+ * TK_ATTN_ERR_DEVICE_TIMEOUT if a kernel abandoned a barrier wait (it then
+ * stops its work early and its outputs are incomplete), or TK_ATTN_ERR_LAUNCH
+ * if the synchronisation itself failed.  Meant for tests and diagnostics.
+ */
+int tk_attn_last_device_error(tk_attn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TK_ATTN_H_ */

@@ -1,0 +1,96 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol ``include/tk_attn.h`` declares, and its host-side argument checks
+return the documented status codes.  No compute calls."""
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "tk_attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tk_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names(tk_lib):
+    assert declared_functions() == sorted(tk_lib.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(tk_lib):
+    lib = tk_lib.library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(tk_lib):
+    assert tk_lib.tk_attn_version() == 10000
+    for code in (0, -1, -2, -3, -4, -5):
+        s = tk_lib.tk_attn_status_string(code)
+        assert s and s != "unknown status"
+    assert tk_lib.tk_attn_status_string(12345) == "unknown status"
+
+
+# Fake, never-dereferenced, 16-byte-aligned addresses far apart.
+Q, K, V, O, L = (1 << 40), (2 << 40), (3 << 40), (4 << 40), (5 << 40)
+
+
+def check(tk_lib, q=Q, k=K, v=V, o=O, lse=L, B=2, H=3, N=100, D=64, scale=0.125, causal=0):
+    return tk_lib.tk_attn_check_args(q, k, v, o, lse, B, H, N, D, scale, causal)
+
+
+def test_valid_arguments(tk_lib):
+    assert check(tk_lib) == tk_lib.TK_ATTN_OK
+    assert check(tk_lib, D=128, causal=1, N=1) == tk_lib.TK_ATTN_OK
+
+
+@pytest.mark.parametrize("kw", [dict(q=0), dict(k=0), dict(v=0), dict(o=0), dict(lse=0),
+                                dict(B=0), dict(H=-1), dict(N=0), dict(scale=0.0),
+                                dict(scale=-1.0), dict(scale=float("inf")),
+                                dict(scale=float("nan"))])
+def test_invalid_arguments(tk_lib, kw):
+    assert check(tk_lib, **kw) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(D=32), dict(D=96), dict(D=256), dict(q=Q + 8),
+                                dict(o=O + 2), dict(lse=L + 4),
+                                dict(B=65536, H=65536, N=1)])
+def test_unsupported_arguments(tk_lib, kw):
+    assert check(tk_lib, **kw) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+
+
+def test_overlapping_outputs_are_rejected(tk_lib):
+    # O [2,3,100,64] bf16 = 76800 bytes; LSE inside it, or O on top of V
+    assert check(tk_lib, lse=O + 1024) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert check(tk_lib, o=V + 16) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert check(tk_lib, lse=Q + 76800 - 16) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    # adjacent but not overlapping is fine
+    assert check(tk_lib, lse=O + 76800) == tk_lib.TK_ATTN_OK
+
+
+def test_fwd_rejects_bad_arguments_before_touching_cuda(tk_lib):
+    # the same validation runs first inside tk_attn_fwd, so no GPU is needed
+    assert tk_lib.tk_attn_fwd(0, K, V, O, L, 1, 1, 16, 64, 0.125, 0, 0) == \
+        tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert tk_lib.tk_attn_fwd(Q, K, V, O, L, 1, 1, 16, 80, 0.125, 0, 0) == \
+        tk_lib.TK_ATTN_ERR_UNSUPPORTED
+
+
+def test_fwd_without_a_gpu_reports_arch(tk_lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert tk_lib.tk_attn_fwd(Q, K, V, O, L, 1, 1, 16, 64, 0.125, 0, 0) == \
+        tk_lib.TK_ATTN_ERR_ARCH
+
+
+def test_binding_raises_when_library_missing(monkeypatch):
+    from attention_forward_tk_gb300 import api
+    monkeypatch.setattr(api, "_lib", None)
+    monkeypatch.setattr(api, "LIB_PATH", "/nonexistent/libtk_attn.so")
+    with pytest.raises(api.TkAttnError):
+        api.library()
