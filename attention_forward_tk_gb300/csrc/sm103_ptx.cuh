@@ -204,14 +204,20 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
       : "memory");
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and an fp32 accumulator.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
-//   15/16 A/B major-ness (0 = K-major, 1 = MN-major), 17-22 N/8, 24-28 M/16.
+// Instruction descriptor for kind::f16 with an fp32 accumulator.
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B must agree), 15/16 A/B major-ness (0 = K-major,
+//   1 = MN-major), 17-22 N/8, 24-28 M/16.
+__host__ __device__ constexpr uint32_t idesc_f32acc(bool bf16, int M, int N, bool a_mn_major,
+                                                    bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+  return idesc_f32acc(true, M, N, a_mn_major, b_mn_major);
 }
 
 // Shared-memory matrix descriptor with the 128-byte swizzle.
@@ -344,6 +350,36 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ uint64_t bf16x2_widen(uint32_t v) {
   return f2_pack(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
+
+// Two fp32 -> packed f16x2 (round to nearest even): `lo` goes to bits 0-15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Per-16-bit-lane unsigned max.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// 2^k for an integer k in [-126, 127], exactly.
+__device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
 
 // Two fp32 -> packed bf16x2 (round to nearest even): `lo` goes to bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

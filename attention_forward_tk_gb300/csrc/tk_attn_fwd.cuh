@@ -17,16 +17,29 @@
 //                 share every K/V tile they load.
 //   warps 0-3   softmax for Q tile 0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax for Q tile 1
-//   warps 8-11  correction: rescale O in TMEM when the row max grows, and the
-//               epilogue O / l -> bf16, LSE
-//   warp 12     tcgen05 MMA issue (one thread) and TMEM allocation
-//   warp 13     TMA producer (one thread): Q tiles, then a K/V ring
-//   warps 14-15 idle (keep the register split warpgroup-aligned)
+//   warps 8-11  V converter (bf16 -> fp16 in shared memory) and epilogue
+//   warp 12     tcgen05 MMA issue for Q tile 0 (one thread; TMEM allocation)
+//   warp 13     tcgen05 MMA issue for Q tile 1 (one thread)
+//   warp 14     TMA producer (one thread): Q tiles, then a K/V ring
+//   warp 15     idle (keeps the register split warpgroup-aligned)
+// One MMA-issuing thread per Q tile: a thread that waits on shared memory
+// after its own tcgen05.commit stalls until its MMAs drain, and the other
+// tile's MMAs keep the tensor core busy through that stall.
+//
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S0 / P0    [128,256) S1 / P1    [256,256+D) O0    [256+D,256+2D) O1
-//   P_t (bf16, two per column) overwrites the first 64 columns of S_t after
-//   the softmax has read S_t; the next S_t MMA is issued after the P_t V MMA,
-//   and the tensor core runs one thread's MMAs in issue order.
+//   P_t (fp16, two per column) overwrites the first 64 columns of S_t after
+//   the softmax has read S_t; the next S_t MMA is issued by the same thread
+//   after the P_t V MMA, and one thread's MMAs run in issue order.
+//
+// Precision: S = Q K^T in bf16 x bf16 -> fp32.  P is rounded to fp16
+// (2^-12 relative, eight times finer than bf16) and multiplied with V in
+// fp16 x fp16 -> fp32; each V tile is converted exactly to fp16 in shared
+// memory, scaled by a power of two 2^E when its magnitudes would overflow
+// fp16 (E is non-increasing along a unit and O is rescaled to match, so the
+// scaling is exact).  The running max is lazy: a row's reference max moves
+// only when the tile max exceeds it by more than 2^8 (log2 units), so P <=
+// 256 and O needs rescaling rarely; the row sum l is accumulated in fp32.
 //
 // Every wait on an mbarrier is bounded; a wait that runs out raises a shared
 // abort flag (all roles then leave their loops), records an error code in a
@@ -61,40 +74,46 @@ struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int kBM = 128;                  // query rows per Q tile
   static constexpr int kBN = 128;                  // keys per K/V tile
-  static constexpr int kUnitRows = 2 * kBM;        // query rows per work unit
-  static constexpr int kTileBytes = kBM * D * 2;   // one Q, K or V tile (bf16)
+  static constexpr int kTileBytes = kBM * D * 2;   // one Q, K or V tile (16-bit)
   static constexpr int kChunks = D / 64;           // 128-byte swizzle column chunks
   static constexpr int kChunkBytes = kBM * 128;    // one chunk: 128 rows x 128 B
-  static constexpr int kStages = D == 128 ? 4 : 8; // K/V ring depth (tiles)
+  static constexpr int kStages = D == 128 ? 4 : 8; // K/V ring depth (tiles; even)
   static constexpr int kSmemBytes = (2 + kStages) * kTileBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
   static constexpr int kThreads = 512;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // converter: 16-byte words of one V tile per converter thread
+  static constexpr int kConvVec = kTileBytes / 16 / 128;
+  static_assert(kStages % 2 == 0, "K tiles in even stages, V tiles in odd stages");
 };
+
+// Lazy-max threshold (log2 units): P stays <= 2^kTau.
+constexpr float kTau = 8.0f;
 
 // Shared-memory bookkeeping that is not tile data.
-struct FwdBarriers {
-  uint64_t q_full[2];     // TMA Q tile landed              (count 1 + tx)
-  uint64_t q_empty;       // all S MMAs of a unit done       (tcgen05.commit)
-  uint64_t kv_full[8];    // TMA K or V tile landed          (count 1 + tx)
-  uint64_t kv_empty[8];   // MMAs reading the stage done     (tcgen05.commit)
-  uint64_t s_full[2];     // S_t = Q_t K^T complete          (tcgen05.commit)
-  uint64_t p_full[2];     // P_t written to TMEM             (4 softmax warps)
-  uint64_t stats_full[2]; // alpha_t written to shared       (4 softmax warps)
-  uint64_t o_ready[2];    // O_t rescaled / drained          (4 correction warps)
-  uint64_t o_full[2];     // last P_t V MMA of a unit done   (tcgen05.commit)
-  uint64_t fin_full[2];   // final m, l of a unit written    (4 softmax warps)
-  uint64_t mma_done;      // every MMA of the CTA complete   (tcgen05.commit)
+struct FwdShared {
+  uint64_t q_full[2];     // TMA Q tile landed                  (1 + tx)
+  uint64_t q_empty;       // S MMAs of both tiles done with Q   (2 commits)
+  uint64_t kv_full[8];    // TMA K or V tile landed             (1 + tx)
+  uint64_t kv_empty[8];   // both tiles' MMAs done with stage   (2 commits)
+  uint64_t v_ready[8];    // V tile converted to fp16           (4 converter warps)
+  uint64_t s_full[2];     // S_t = Q_t K^T complete             (commit)
+  uint64_t p_full[2];     // P_t in TMEM, O_t rescaled          (4 softmax warps)
+  uint64_t fin_full[2];   // final m, l of a unit in shared     (4 softmax warps)
+  uint64_t o_full[2];     // last P_t V MMA of a unit done      (commit)
+  uint64_t o_free[2];     // epilogue has read O_t              (4 converter warps)
+  uint64_t conv_bar;      // converter warps' tile-max exchange (4 converter warps)
+  uint64_t mma_done[2];   // every MMA of one issuing thread done (commit)
   uint32_t tmem_base;
   int abort;
-  float alpha[2][128];        // per-row rescale factor of the current step
-  float m_fin[2][2][128];     // [unit parity][tile][row] final scaled-log2 max
-  float l_fin[2][2][128];     // [unit parity][tile][row] final row sum of P
-  float lt_fin[2][2][128];    // [unit parity][tile][row] same, of bf16-rounded P
+  int v_exp[8];           // power-of-two exponent of each converted V stage
+  uint32_t conv_max[2][4];
+  float m_fin[2][2][128];  // [unit parity][tile][row] final reference max (scaled log2)
+  float l_fin[2][2][128];  // [unit parity][tile][row] final row sum
 };
 
-__device__ __forceinline__ void raise_abort(FwdBarriers &sb, int *err, int code) {
+__device__ __forceinline__ void raise_abort(FwdShared &sb, int *err, int code) {
   sb.abort = 1;
   atomicCAS(err, 0, code);
 }
@@ -127,7 +146,7 @@ __global__ void __launch_bounds__(512, 1)
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ FwdBarriers sb;
+  __shared__ FwdShared sb;
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sQ = smem;                        // 2 tiles
@@ -142,17 +161,18 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.q_full[t], 1);
       mbar_init(&sb.s_full[t], 1);
       mbar_init(&sb.p_full[t], 4);
-      mbar_init(&sb.stats_full[t], 4);
-      mbar_init(&sb.o_ready[t], 4);
-      mbar_init(&sb.o_full[t], 1);
       mbar_init(&sb.fin_full[t], 4);
+      mbar_init(&sb.o_full[t], 1);
+      mbar_init(&sb.o_free[t], 4);
+      mbar_init(&sb.mma_done[t], 1);
     }
-    mbar_init(&sb.q_empty, 1);
+    mbar_init(&sb.q_empty, 2);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sb.kv_full[s], 1);
-      mbar_init(&sb.kv_empty[s], 1);
+      mbar_init(&sb.kv_empty[s], 2);
+      mbar_init(&sb.v_ready[s], 4);
     }
-    mbar_init(&sb.mma_done, 1);
+    mbar_init(&sb.conv_bar, 4);
     sb.abort = 0;
     fence_mbar_init();
   }
@@ -160,7 +180,7 @@ __global__ void __launch_bounds__(512, 1)
     tmem_alloc(&sb.tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 13 && lane == 0) {
+  if (warp == 14 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -172,19 +192,24 @@ __global__ void __launch_bounds__(512, 1)
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;\n" ::: "memory");
     const int t = warp >> 2;                 // Q tile
     const int row = (warp & 3) * 32 + lane;  // row in tile == TMEM lane
-    const uint32_t tS = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (t ? C::kColS1 : C::kColS0);
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
+    const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
     const float c = p.scale_log2;
     uint32_t s_phase = 0;
+    uint32_t kvb = 0;  // K/V load index of this unit's K_0
     int uc = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
       int bh, mb;
       unit_coords(p, kCausal, u, bh, mb);
       const int n_t = kv_tiles(p, kCausal, mb, t);
+      const int n1 = kv_tiles(p, kCausal, mb, 1);
       const int qrow = mb * 256 + t * 128 + row;  // global query index
-      float m_run = -INFINITY, l_run = 0.f, lt_run = 0.f;
+      float m_run = -INFINITY, l_run = 0.f;
+      int e_cur = 0;  // V exponent O is accumulated at
       for (int j = 0; j < n_t; ++j) {
         if (!mbar_wait(&sb.s_full[t], s_phase, abort_flag)) {
           raise_abort(sb, p.err, kDevErrTimeout);
@@ -218,17 +243,29 @@ __global__ void __launch_bounds__(512, 1)
           mx0 = max3(mx0, __uint_as_float(s[i]), __uint_as_float(s[i + 1]));
           mx1 = max3(mx1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
         }
-        const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * c);
-        const float alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
-        sb.alpha[t][row] = alpha;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sb.stats_full[t]);
-        // P = 2^(s*c - m_new).  Two row sums: of the fp32 P (for the LSE) and
-        // of the bf16-rounded P the P V MMA consumes (for normalising O, so
-        // the weights applied to V sum to one exactly as used).
+        const float m_cand = fmaxf(mx0, mx1) * c;
+        // Lazy max: move the reference only when the tile max exceeds it by
+        // more than kTau (always on the first tile, where m_run = -inf).
+        const bool grow = m_cand > m_run + kTau;
+        const float m_new = grow ? m_cand : m_run;
+        const float fac = grow ? ex2_approx(m_run - m_new) : 1.0f;  // 0 on the first tile
+        // Exponent of the V tile this step multiplies (set by the converter).
+        const uint32_t vidx = kvb + 2 * j + 1;
+        if (!mbar_wait(&sb.v_ready[vidx % C::kStages], (vidx / C::kStages) & 1, abort_flag)) {
+          raise_abort(sb, p.err, kDevErrTimeout);
+          goto done;
+        }
+        const int e_j = sb.v_exp[vidx % C::kStages];
+        // O_t must be multiplied by this factor before the P_t V MMA of this
+        // step: the reference max moved, or V_j was scaled by a smaller 2^e.
+        const float ofac = (e_j == e_cur) ? fac : fac * exp2i(e_j - e_cur);
+        e_cur = e_j;
+        m_run = m_new;
+        // P = 2^(s*c - m_run) <= 2^kTau, rounded to fp16 for the P V MMA;
+        // the row sum is taken over the fp32 P.
         const uint64_t c2 = f2_pack(c, c);
-        const uint64_t nm2 = f2_pack(-m_new, -m_new);
-        uint64_t la = 0, lb = 0, lta = 0, ltb = 0;  // (+0.f, +0.f) pairs
+        const uint64_t nm2 = f2_pack(-m_run, -m_run);
+        uint64_t la = 0, lb = 0;  // (+0.f, +0.f) pairs
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
@@ -241,27 +278,44 @@ __global__ void __launch_bounds__(512, 1)
                     x2, x3);
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          pk[i] = pack_bf16x2(p0, p1);
-          pk[i + 1] = pack_bf16x2(p2, p3);
+          pk[i] = pack_f16x2(p0, p1);
+          pk[i + 1] = pack_f16x2(p2, p3);
           la = f2_add(la, f2_pack(p0, p1));
           lb = f2_add(lb, f2_pack(p2, p3));
-          lta = f2_add(lta, bf16x2_widen(pk[i]));
-          ltb = f2_add(ltb, bf16x2_widen(pk[i + 1]));
         }
         tmem_st_32x32b_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
         tmem_st_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(f2_add(la, lb), a0, a1);
-          f2_unpack(f2_add(lta, ltb), b0, b1);
-          l_run = l_run * alpha + (a0 + a1);
-          lt_run = lt_run * alpha + (b0 + b1);
+        // Rescale this warp's O rows (after the scores are dead, to keep
+        // register pressure down).  S_t of this step is complete, and its
+        // commit covers the previous P_t V MMA: O_t holds its accumulated value.
+        if (j > 0 && __any_sync(0xffffffffu, ofac != 1.0f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tO + c0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              reg_barrier(r[i]);
+              reg_barrier(r[i + 1]);
+              float a, b;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                               f2_pack(ofac, ofac)),
+                        a, b);
+              r[i] = __float_as_uint(a);
+              r[i + 1] = __float_as_uint(b);
+            }
+            tmem_st_32x32b_x32(tO + c0, r);
+          }
         }
-        m_run = m_new;
+        {
+          float a0, a1;
+          f2_unpack(f2_add(la, lb), a0, a1);
+          l_run = l_run * fac + (a0 + a1);
+        }
         if (j == n_t - 1) {
           sb.m_fin[uc & 1][t][row] = m_run;
           sb.l_fin[uc & 1][t][row] = l_run;
-          sb.lt_fin[uc & 1][t][row] = lt_run;
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -271,195 +325,231 @@ __global__ void __launch_bounds__(512, 1)
           if (j == n_t - 1) mbar_arrive(&sb.fin_full[t]);
         }
       }
+      kvb += 2 * n1;
     }
   } else if (warp < 12) {
-    // ------------------------------------------------------------ correction + epilogue
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
-    const int row = (warp & 3) * 32 + lane;
+    // ------------------------------------------------------------ V converter + epilogue
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory");
+    const int cw = warp - 8;                 // converter warp 0..3
+    const int ct = threadIdx.x - 256;        // converter thread 0..127
+    const int row = (warp & 3) * 32 + lane;  // epilogue: row == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    uint32_t st_phase[2] = {0, 0};
-    uint32_t ofull_phase[2] = {0, 0};
+    uint32_t kvb = 0;
+    uint32_t conv_count = 0;  // V tiles converted (conv_bar phases)
+    // the unit whose epilogue is pending
+    int pend_bh = -1, pend_mb = 0, pend_uc = 0, pend_e[2] = {0, 0};
     int uc = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
-      int bh, mb;
-      unit_coords(p, kCausal, u, bh, mb);
-      const int n0 = kv_tiles(p, kCausal, mb, 0);
-      const int n1 = kv_tiles(p, kCausal, mb, 1);
-      for (int j = 0; j < n1; ++j) {
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (j >= (t ? n1 : n0)) continue;
-          if (!mbar_wait(&sb.stats_full[t], st_phase[t], abort_flag)) {
-            raise_abort(sb, p.err, kDevErrTimeout);
-            goto done;
-          }
-          st_phase[t] ^= 1;
-          if (j > 0) {
-            const float alpha = sb.alpha[t][row];
-            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-              // S_t of this step is complete, and its commit covers the
-              // previous P_t V MMA: O_t holds its accumulated value.
-              tc_fence_after_sync();
-              const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
-#pragma unroll
-              for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tO + c0, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  reg_barrier(r[i]);
-                  r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                }
-                tmem_st_32x32b_x32(tO + c0, r);
-              }
-              tmem_wait_st();
-            }
-          }
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sb.o_ready[t]);
-        }
+    for (int u = blockIdx.x;; u += gridDim.x, ++uc) {
+      const bool have_unit = u < p.num_units;
+      int bh = 0, mb = 0, n0 = 0, n1 = 0;
+      if (have_unit) {
+        unit_coords(p, kCausal, u, bh, mb);
+        n0 = kv_tiles(p, kCausal, mb, 0);
+        n1 = kv_tiles(p, kCausal, mb, 1);
       }
-      // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
+      int e_run = 0, e_t0 = 0, e_t1 = 0;
+      for (int j = 0; j <= n1; ++j) {
+        // The previous unit's epilogue runs after this unit's first V tile
+        // is converted (so its P V MMAs can start), or at the very end.
+        if (pend_bh >= 0 && (j == 1 || !have_unit)) {
+#pragma unroll 1
+          for (int t = 0; t < 2; ++t) {
+            if (!mbar_wait(&sb.fin_full[t], pend_uc & 1, abort_flag) ||
+                !mbar_wait(&sb.o_full[t], pend_uc & 1, abort_flag)) {
+              raise_abort(sb, p.err, kDevErrTimeout);
+              goto done;
+            }
+            tc_fence_after_sync();
+            const float m = sb.m_fin[pend_uc & 1][t][row];
+            const float l = sb.l_fin[pend_uc & 1][t][row];
+            const float oscale = exp2i(-pend_e[t]) / l;
+            const int qrow = pend_mb * 256 + t * 128 + row;
+            const bool valid = qrow < p.N;
+            __nv_bfloat16 *orow = p.o + ((size_t)pend_bh * p.N + (valid ? qrow : 0)) * D;
+            const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (!mbar_wait(&sb.fin_full[t], uc & 1, abort_flag) ||
-            !mbar_wait(&sb.o_full[t], ofull_phase[t], abort_flag)) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(tO + c0, r);
+              tmem_wait_ld();
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                reg_barrier(r[2 * i]);
+                reg_barrier(r[2 * i + 1]);
+                pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * oscale,
+                                    __uint_as_float(r[2 * i + 1]) * oscale);
+              }
+              if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              }
+            }
+            if (valid)
+              p.lse[(size_t)pend_bh * p.N + qrow] = (m + lg2_approx(l)) * 0.69314718055994531f;
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sb.o_free[t]);
+          }
+          pend_bh = -1;
+        }
+        if (j == n1) break;
+        // Convert V_j (bf16 -> fp16, in place, scaled by 2^e_run).
+        const uint32_t vidx = kvb + 2 * j + 1;
+        const uint32_t st = vidx % C::kStages;
+        if (!mbar_wait(&sb.kv_full[st], (vidx / C::kStages) & 1, abort_flag)) {
           raise_abort(sb, p.err, kDevErrTimeout);
           goto done;
         }
-        ofull_phase[t] ^= 1;
-        tc_fence_after_sync();
-        const float m = sb.m_fin[uc & 1][t][row];
-        const float l = sb.l_fin[uc & 1][t][row];
-        const float inv_l = 1.0f / sb.lt_fin[uc & 1][t][row];
-        const int qrow = mb * 256 + t * 128 + row;
-        const bool valid = qrow < p.N;
-        __nv_bfloat16 *orow = p.o + ((size_t)bh * p.N + (valid ? qrow : 0)) * D;
-        const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
+        uint4 *tile = reinterpret_cast<uint4 *>(sKV + st * C::kTileBytes);
+        uint4 w[C::kConvVec];
+        uint32_t amax2 = 0;  // per-16-bit-lane max of |bf16| bit patterns
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tO + c0, r);
-          tmem_wait_ld();
-          uint32_t pk[16];
+        for (int i = 0; i < C::kConvVec; ++i) {
+          w[i] = tile[ct + 128 * i];
+          amax2 = max_u16x2(amax2, w[i].x & 0x7fff7fffu);
+          amax2 = max_u16x2(amax2, w[i].y & 0x7fff7fffu);
+          amax2 = max_u16x2(amax2, w[i].z & 0x7fff7fffu);
+          amax2 = max_u16x2(amax2, w[i].w & 0x7fff7fffu);
+        }
+        const uint32_t wmax =
+            __reduce_max_sync(0xffffffffu, max(amax2 & 0xffffu, amax2 >> 16));
+        if (lane == 0) {
+          sb.conv_max[conv_count & 1][cw] = wmax;
+          mbar_arrive(&sb.conv_bar);
+        }
+        if (!mbar_wait(&sb.conv_bar, conv_count & 1, abort_flag)) {
+          raise_abort(sb, p.err, kDevErrTimeout);
+          goto done;
+        }
+        const uint32_t amax = max(max(sb.conv_max[conv_count & 1][0], sb.conv_max[conv_count & 1][1]),
+                                  max(sb.conv_max[conv_count & 1][2], sb.conv_max[conv_count & 1][3]));
+        ++conv_count;
+        // |v| < 2^(k+1) with k = biased exponent - 127.  fp16 holds every
+        // bf16 value below 2^16 exactly; scale larger tiles down by 2^(15-k).
+        // Non-finite inputs (exponent field 255) are passed through unscaled.
+        const int kexp = (int)(amax >> 7) - 127;
+        if (amax < 0x7f80u && kexp >= 16) e_run = min(e_run, 15 - kexp);
+        if (e_run == 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            reg_barrier(r[2 * i]);
-            reg_barrier(r[2 * i + 1]);
-            pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
-                                __uint_as_float(r[2 * i + 1]) * inv_l);
+          for (int i = 0; i < C::kConvVec; ++i) {
+            uint4 o;
+            o.x = pack_f16x2(__uint_as_float(w[i].x << 16), __uint_as_float(w[i].x & 0xffff0000u));
+            o.y = pack_f16x2(__uint_as_float(w[i].y << 16), __uint_as_float(w[i].y & 0xffff0000u));
+            o.z = pack_f16x2(__uint_as_float(w[i].z << 16), __uint_as_float(w[i].z & 0xffff0000u));
+            o.w = pack_f16x2(__uint_as_float(w[i].w << 16), __uint_as_float(w[i].w & 0xffff0000u));
+            tile[ct + 128 * i] = o;
           }
-          if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+        } else {
+          const float sc = exp2i(e_run);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < C::kConvVec; ++i) {
+            uint4 o;
+            o.x = pack_f16x2(__uint_as_float(w[i].x << 16) * sc,
+                             __uint_as_float(w[i].x & 0xffff0000u) * sc);
+            o.y = pack_f16x2(__uint_as_float(w[i].y << 16) * sc,
+                             __uint_as_float(w[i].y & 0xffff0000u) * sc);
+            o.z = pack_f16x2(__uint_as_float(w[i].z << 16) * sc,
+                             __uint_as_float(w[i].z & 0xffff0000u) * sc);
+            o.w = pack_f16x2(__uint_as_float(w[i].w << 16) * sc,
+                             __uint_as_float(w[i].w & 0xffff0000u) * sc);
+            tile[ct + 128 * i] = o;
           }
         }
-        if (valid) p.lse[(size_t)bh * p.N + qrow] = (m + lg2_approx(l)) * 0.69314718055994531f;
-        // O_t has been read out: the next unit may overwrite it.  (Its first
-        // P_t V MMA also waits on the o_ready arrival of step 0 above.)
+        fence_proxy_async_smem();  // the generic writes become visible to the tensor core
+        if (ct == 0) sb.v_exp[st] = e_run;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sb.v_ready[st]);
+        if (j == n0 - 1) e_t0 = e_run;
+        if (j == n1 - 1) e_t1 = e_run;
       }
+      if (!have_unit) break;
+      pend_bh = bh;
+      pend_mb = mb;
+      pend_uc = uc;
+      pend_e[0] = e_t0;
+      pend_e[1] = e_t1;
+      kvb += 2 * n1;
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
-    if (warp == 12 && lane == 0) {
-      // ---------------------------------------------------------- MMA issue
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      const uint32_t sQ_addr = smem_addr(sQ);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 48;\n" ::: "memory");
+    if ((warp == 12 || warp == 13) && lane == 0) {
+      // ---------------------------------------------------------- MMA issue (one Q tile)
+      const int t = warp - 12;
+      constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);  // bf16 Q, K
+      constexpr uint32_t idO = idesc_f32acc(false, 128, D, false, true);    // fp16 P, V
+      const uint32_t qbase = smem_addr(sQ) + t * C::kTileBytes;
       const uint32_t sKV_addr = smem_addr(sKV);
-      uint32_t q_phase = 0, p_phase[2] = {0, 0}, or_phase[2] = {0, 0};
-      uint32_t kv_idx = 0;  // loads consumed so far (K_0, V_0, K_1, ...)
-      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+      const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
+      const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
+      uint32_t p_phase = 0;
+      uint32_t kvb = 0;
+      int uc = 0;
+      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
         int bh, mb;
         unit_coords(p, kCausal, u, bh, mb);
-        const int n0 = kv_tiles(p, kCausal, mb, 0);
+        const int n_t = kv_tiles(p, kCausal, mb, t);
         const int n1 = kv_tiles(p, kCausal, mb, 1);
-        if (!mbar_wait(&sb.q_full[0], q_phase, abort_flag) ||
-            !mbar_wait(&sb.q_full[1], q_phase, abort_flag)) {
+        if (!mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) {
           raise_abort(sb, p.err, kDevErrTimeout);
           goto mma_exit;
         }
-        q_phase ^= 1;
         tc_fence_after_sync();
-        uint32_t k_stage = 0, v_stage = 0;
-        // Issue order per step j: P0 V_{j-1}, S0 = Q0 K_j^T, P1 V_{j-1},
-        // S1 = Q1 K_j^T.  Each softmax then has the other tile's two MMAs
-        // (about 1024 tensor-core clocks) to turn S into P.
-        for (int j = 0; j <= n1; ++j) {
 #pragma unroll 1
-          for (int t = 0; t < 2; ++t) {
-            const int n_t = t ? n1 : n0;
-            if (j >= 1 && j <= n_t) {
-              // O_t += P_t V_{j-1}
-              if (!mbar_wait(&sb.p_full[t], p_phase[t], abort_flag) ||
-                  !mbar_wait(&sb.o_ready[t], or_phase[t], abort_flag)) {
-                raise_abort(sb, p.err, kDevErrTimeout);
-                goto mma_exit;
-              }
-              p_phase[t] ^= 1;
-              or_phase[t] ^= 1;
-              tc_fence_after_sync();
-              const uint32_t tP = tmem + (t ? C::kColS1 : C::kColS0);
-              const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
-              const uint32_t vbase = sKV_addr + v_stage * C::kTileBytes;
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_bf16_ts(tO, tP + kk * 8,
-                             sdesc_sw128(vbase + kk * 2048, C::kChunkBytes, 1024), idO,
-                             (j > 1 || kk > 0) ? 1u : 0u);
-              if (j == n_t) umma_commit(&sb.o_full[t]);
-              if (t == 1) umma_commit(&sb.kv_empty[v_stage]);  // V_{j-1} fully used
+        for (int j = 0; j < n1; ++j) {
+          const uint32_t kidx = kvb + 2 * j, vidx = kidx + 1;
+          const uint32_t ks = kidx % C::kStages, vs = vidx % C::kStages;
+          if (j < n_t) {
+            // S_t = Q_t K_j^T
+            if (!mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag)) {
+              raise_abort(sb, p.err, kDevErrTimeout);
+              goto mma_exit;
             }
-            if (j < n_t) {
-              if (t == 0 || j >= n0) {
-                // first user of K_j in this step waits for it
-                k_stage = kv_idx % C::kStages;
-                if (!mbar_wait(&sb.kv_full[k_stage], (kv_idx / C::kStages) & 1, abort_flag)) {
-                  raise_abort(sb, p.err, kDevErrTimeout);
-                  goto mma_exit;
-                }
-                ++kv_idx;
-                tc_fence_after_sync();
-              }
-              // S_t = Q_t K_j^T
-              const uint32_t qbase = sQ_addr + t * C::kTileBytes;
-              const uint32_t kbase = sKV_addr + k_stage * C::kTileBytes;
-              const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
+            tc_fence_after_sync();
+            const uint32_t kbase = sKV_addr + ks * C::kTileBytes;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                umma_bf16_ss(tS, sdesc_sw128(qbase + off, 16, 1024),
-                             sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
-              }
-              umma_commit(&sb.s_full[t]);
-              if (t == 1) {
-                umma_commit(&sb.kv_empty[k_stage]);  // K_j fully used
-                if (j == n1 - 1) umma_commit(&sb.q_empty);
-                // V_j, needed by the next step's P V MMAs
-                v_stage = kv_idx % C::kStages;
-                if (!mbar_wait(&sb.kv_full[v_stage], (kv_idx / C::kStages) & 1, abort_flag)) {
-                  raise_abort(sb, p.err, kDevErrTimeout);
-                  goto mma_exit;
-                }
-                ++kv_idx;
-                tc_fence_after_sync();
-              }
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+              umma_bf16_ss(tS, sdesc_sw128(qbase + off, 16, 1024),
+                           sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
             }
+            umma_commit(&sb.s_full[t]);
+            if (j == n_t - 1) umma_commit(&sb.q_empty);
           }
+          umma_commit(&sb.kv_empty[ks]);  // this tile is done with K_j
+          if (j < n_t) {
+            // O_t (+)= P_t V_j, once the softmax has written P_t (and
+            // rescaled O_t), V_j is in fp16, and the epilogue of the previous
+            // unit has drained O_t.
+            if ((j == 0 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
+                !mbar_wait(&sb.p_full[t], p_phase, abort_flag) ||
+                !mbar_wait(&sb.v_ready[vs], (vidx / C::kStages) & 1, abort_flag)) {
+              raise_abort(sb, p.err, kDevErrTimeout);
+              goto mma_exit;
+            }
+            p_phase ^= 1;
+            tc_fence_after_sync();
+            const uint32_t vbase = sKV_addr + vs * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::kChunkBytes, 1024),
+                           idO, (j > 0 || kk > 0) ? 1u : 0u);
+            if (j == n_t - 1) umma_commit(&sb.o_full[t]);
+          }
+          umma_commit(&sb.kv_empty[vs]);  // this tile is done with V_j
         }
+        kvb += 2 * n1;
       }
     mma_exit:
       // every MMA this thread issued must finish before the TMEM is freed
-      umma_commit(&sb.mma_done);
+      umma_commit(&sb.mma_done[t]);
       {
         int never = 0;
-        mbar_wait(&sb.mma_done, 0, &never);
+        mbar_wait(&sb.mma_done[t], 0, &never);
       }
-    } else if (warp == 13 && lane == 0) {
+    } else if (warp == 14 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       uint32_t kv_idx = 0;
       uint32_t q_loads = 0;  // Q tile pairs issued
