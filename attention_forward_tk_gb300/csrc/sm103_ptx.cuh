@@ -58,10 +58,24 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 // Wait until the phase with the given parity has completed.  Returns false
 // if the wait was abandoned: the limit ran out or another thread of the CTA
 // already raised `abort_flag` (a shared-memory word).  Never traps.
+__device__ __forceinline__ bool mbar_test_wait_addr(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           volatile int *abort_flag) {
   const uint32_t a = smem_addr(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  // A non-blocking probe first: far cheaper than try_wait when the phase
+  // has already completed, which is the common case on the hot path.
+  if (mbar_test_wait_addr(a, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;

@@ -105,6 +105,7 @@ struct FwdShared {
   uint64_t o_free[2];     // epilogue has read O_t              (4 converter warps)
   uint64_t conv_bar;      // converter warps' tile-max exchange (4 converter warps)
   uint64_t mma_done[2];   // every MMA of one issuing thread done (commit)
+  uint64_t turn[2];       // issuing thread t may issue its next group (1 arrive)
   uint32_t tmem_base;
   int abort;
   int v_exp[8];           // power-of-two exponent of each converted V stage
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.o_full[t], 1);
       mbar_init(&sb.o_free[t], 4);
       mbar_init(&sb.mma_done[t], 1);
+      mbar_init(&sb.turn[t], 1);
     }
     mbar_init(&sb.q_empty, 2);
     for (int s = 0; s < C::kStages; ++s) {
@@ -236,14 +238,17 @@ __global__ void __launch_bounds__(512, 1)
             if (i >= lim) s[i] = __float_as_uint(-INFINITY);
         }
         // Row max of the raw scores; scale > 0 so max(s)*c = max(s*c).
-        float mx0 = fmaxf(__uint_as_float(s[0]), __uint_as_float(s[1]));
-        float mx1 = fmaxf(__uint_as_float(s[2]), __uint_as_float(s[3]));
+        float mx[8];
 #pragma unroll
-        for (int i = 4; i < 128; i += 4) {
-          mx0 = max3(mx0, __uint_as_float(s[i]), __uint_as_float(s[i + 1]));
-          mx1 = max3(mx1, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1]));
+#pragma unroll
+        for (int i = 16; i < 128; i += 16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            mx[q] = max3(mx[q], __uint_as_float(s[i + 2 * q]), __uint_as_float(s[i + 2 * q + 1]));
         }
-        const float m_cand = fmaxf(mx0, mx1) * c;
+        const float m_cand =
+            fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], max3(mx[5], mx[6], mx[7]))) * c;
         // Lazy max: move the reference only when the tile max exceeds it by
         // more than kTau (always on the first tile, where m_run = -inf).
         const bool grow = m_cand > m_run + kTau;
@@ -477,6 +482,12 @@ __global__ void __launch_bounds__(512, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 48;\n" ::: "memory");
     if ((warp == 12 || warp == 13) && lane == 0) {
       // ---------------------------------------------------------- MMA issue (one Q tile)
+      // Step j of a unit issues this tile's group [P_t V_{j-1}, Q_t K_j^T].
+      // The two issuing threads take turns (turn[] barriers), so the tensor
+      // core runs P0 V, S0, P1 V, S1, P0 V, ... and each softmax works while
+      // the other tile's two MMAs run.  A thread hands the turn over before
+      // its commits, and its post-commit stall lands on its next turn wait,
+      // while the other thread's MMAs keep the tensor core busy.
       const int t = warp - 12;
       constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);  // bf16 Q, K
       constexpr uint32_t idO = idesc_f32acc(false, 128, D, false, true);    // fp16 P, V
@@ -484,7 +495,8 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t sKV_addr = smem_addr(sKV);
       const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
       const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
-      uint32_t p_phase = 0;
+      uint32_t p_phase = 0, turn_phase = 0;
+      bool first_group = true;
       uint32_t kvb = 0;
       int uc = 0;
       for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
@@ -492,38 +504,25 @@ __global__ void __launch_bounds__(512, 1)
         unit_coords(p, kCausal, u, bh, mb);
         const int n_t = kv_tiles(p, kCausal, mb, t);
         const int n1 = kv_tiles(p, kCausal, mb, 1);
-        if (!mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) {
-          raise_abort(sb, p.err, kDevErrTimeout);
-          goto mma_exit;
-        }
-        tc_fence_after_sync();
 #pragma unroll 1
-        for (int j = 0; j < n1; ++j) {
-          const uint32_t kidx = kvb + 2 * j, vidx = kidx + 1;
-          const uint32_t ks = kidx % C::kStages, vs = vidx % C::kStages;
-          if (j < n_t) {
-            // S_t = Q_t K_j^T
-            if (!mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag)) {
+        for (int j = 0; j <= n1; ++j) {
+          if (!(t == 0 && first_group)) {
+            if (!mbar_wait(&sb.turn[t], turn_phase, abort_flag)) {
               raise_abort(sb, p.err, kDevErrTimeout);
               goto mma_exit;
             }
-            tc_fence_after_sync();
-            const uint32_t kbase = sKV_addr + ks * C::kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-              umma_bf16_ss(tS, sdesc_sw128(qbase + off, 16, 1024),
-                           sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&sb.s_full[t]);
-            if (j == n_t - 1) umma_commit(&sb.q_empty);
+            turn_phase ^= 1;
           }
-          umma_commit(&sb.kv_empty[ks]);  // this tile is done with K_j
-          if (j < n_t) {
-            // O_t (+)= P_t V_j, once the softmax has written P_t (and
-            // rescaled O_t), V_j is in fp16, and the epilogue of the previous
-            // unit has drained O_t.
-            if ((j == 0 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
+          first_group = false;
+          const bool do_pv = j >= 1 && j <= n_t;
+          const bool do_s = j < n_t;
+          const uint32_t kidx = kvb + 2 * j, vidx = kidx - 1;  // K_j and V_{j-1}
+          const uint32_t ks = kidx % C::kStages, vs = vidx % C::kStages;
+          if (do_pv) {
+            // O_t (+)= P_t V_{j-1}, once the softmax has written P_t (and
+            // rescaled O_t), V_{j-1} is in fp16, and the previous unit's
+            // epilogue has drained O_t.
+            if ((j == 1 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
                 !mbar_wait(&sb.p_full[t], p_phase, abort_flag) ||
                 !mbar_wait(&sb.v_ready[vs], (vidx / C::kStages) & 1, abort_flag)) {
               raise_abort(sb, p.err, kDevErrTimeout);
@@ -535,10 +534,32 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               umma_bf16_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::kChunkBytes, 1024),
-                           idO, (j > 0 || kk > 0) ? 1u : 0u);
-            if (j == n_t - 1) umma_commit(&sb.o_full[t]);
+                           idO, (j > 1 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&sb.kv_empty[vs]);  // this tile is done with V_j
+          if (do_s) {
+            // S_t = Q_t K_j^T
+            if ((j == 0 && !mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) ||
+                !mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag)) {
+              raise_abort(sb, p.err, kDevErrTimeout);
+              goto mma_exit;
+            }
+            tc_fence_after_sync();
+            const uint32_t kbase = sKV_addr + ks * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+              umma_bf16_ss(tS, sdesc_sw128(qbase + off, 16, 1024),
+                           sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            }
+          }
+          mbar_arrive(&sb.turn[1 - t]);  // the other tile's thread may issue now
+          if (do_s) {
+            umma_commit(&sb.s_full[t]);
+            if (j == n_t - 1) umma_commit(&sb.q_empty);
+          }
+          if (do_pv && j == n_t) umma_commit(&sb.o_full[t]);
+          if (j >= 1) umma_commit(&sb.kv_empty[vs]);  // this tile is done with V_{j-1}
+          if (j < n1) umma_commit(&sb.kv_empty[ks]);  // ... and with K_j
         }
         kvb += 2 * n1;
       }
