@@ -18,19 +18,19 @@
 //   warps 0-3   softmax for Q tile 0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax for Q tile 1
 //   warps 8-11  V converter (bf16 -> fp16 in shared memory) and epilogue
-//   warp 12     tcgen05 MMA issue for Q tile 0 (one thread; TMEM allocation)
-//   warp 13     tcgen05 MMA issue for Q tile 1 (one thread)
+//   warp 12     tcgen05 MMA issue (one thread) and TMEM allocation
 //   warp 14     TMA producer (one thread): Q tiles, then a K/V ring
-//   warp 15     idle (keeps the register split warpgroup-aligned)
-// One MMA-issuing thread per Q tile: a thread that waits on shared memory
-// after its own tcgen05.commit stalls until its MMAs drain, and the other
-// tile's MMAs keep the tensor core busy through that stall.
+//   warps 13,15 idle (keep the register split warpgroup-aligned)
+// The MMA thread issues, per K/V step, P0 V, S0, P1 V, S1: each softmax
+// warpgroup works while the other tile's two MMAs run.  A thread that waits
+// on shared memory after its own tcgen05.commit stalls until the tensor pipe
+// drains, so the MMA thread waits at only the two points a step needs.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S0 / P0    [128,256) S1 / P1    [256,256+D) O0    [256+D,256+2D) O1
 //   P_t (fp16, two per column) overwrites the first 64 columns of S_t after
-//   the softmax has read S_t; the next S_t MMA is issued by the same thread
-//   after the P_t V MMA, and one thread's MMAs run in issue order.
+//   the softmax has read S_t; the next S_t MMA is issued after the P_t V MMA
+//   by the same thread, and one thread's MMAs run in issue order.
 //
 // Precision: S = Q K^T in bf16 x bf16 -> fp32.  P is rounded to fp16
 // (2^-12 relative, eight times finer than bf16) and multiplied with V in
@@ -94,9 +94,9 @@ constexpr float kTau = 8.0f;
 // Shared-memory bookkeeping that is not tile data.
 struct FwdShared {
   uint64_t q_full[2];     // TMA Q tile landed                  (1 + tx)
-  uint64_t q_empty;       // S MMAs of both tiles done with Q   (2 commits)
+  uint64_t q_empty;       // S MMAs of both tiles done with Q   (commit)
   uint64_t kv_full[8];    // TMA K or V tile landed             (1 + tx)
-  uint64_t kv_empty[8];   // both tiles' MMAs done with stage   (2 commits)
+  uint64_t kv_empty[8];   // both tiles' MMAs done with stage   (commit)
   uint64_t v_ready[8];    // V tile converted to fp16           (4 converter warps)
   uint64_t s_full[2];     // S_t = Q_t K^T complete             (commit)
   uint64_t p_full[2];     // P_t in TMEM, O_t rescaled          (4 softmax warps)
@@ -104,8 +104,7 @@ struct FwdShared {
   uint64_t o_full[2];     // last P_t V MMA of a unit done      (commit)
   uint64_t o_free[2];     // epilogue has read O_t              (4 converter warps)
   uint64_t conv_bar;      // converter warps' tile-max exchange (4 converter warps)
-  uint64_t mma_done[2];   // every MMA of one issuing thread done (commit)
-  uint64_t turn[2];       // issuing thread t may issue its next group (1 arrive)
+  uint64_t mma_done[2];   // every MMA of the issuing thread done (commit; [0] used)
   uint32_t tmem_base;
   int abort;
   int v_exp[8];           // power-of-two exponent of each converted V stage
@@ -166,12 +165,11 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.o_full[t], 1);
       mbar_init(&sb.o_free[t], 4);
       mbar_init(&sb.mma_done[t], 1);
-      mbar_init(&sb.turn[t], 1);
     }
-    mbar_init(&sb.q_empty, 2);
+    mbar_init(&sb.q_empty, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sb.kv_full[s], 1);
-      mbar_init(&sb.kv_empty[s], 2);
+      mbar_init(&sb.kv_empty[s], 1);
       mbar_init(&sb.v_ready[s], 4);
     }
     mbar_init(&sb.conv_bar, 4);
@@ -334,7 +332,7 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ V converter + epilogue
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;\n" ::: "memory");
     const int cw = warp - 8;                 // converter warp 0..3
     const int ct = threadIdx.x - 256;        // converter thread 0..127
     const int row = (warp & 3) * 32 + lane;  // epilogue: row == TMEM lane
@@ -479,96 +477,95 @@ __global__ void __launch_bounds__(512, 1)
       kvb += 2 * n1;
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 48;\n" ::: "memory");
-    if ((warp == 12 || warp == 13) && lane == 0) {
-      // ---------------------------------------------------------- MMA issue (one Q tile)
-      // Step j of a unit issues this tile's group [P_t V_{j-1}, Q_t K_j^T].
-      // The two issuing threads take turns (turn[] barriers), so the tensor
-      // core runs P0 V, S0, P1 V, S1, P0 V, ... and each softmax works while
-      // the other tile's two MMAs run.  A thread hands the turn over before
-      // its commits, and its post-commit stall lands on its next turn wait,
-      // while the other thread's MMAs keep the tensor core busy.
-      const int t = warp - 12;
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+    if (warp == 12 && lane == 0) {
+      // ---------------------------------------------------------- MMA issue
+      // Step j issues P0 V_{j-1}, S0 = Q0 K_j^T, then P1 V_{j-1}, S1 = Q1 K_j^T,
+      // so each softmax warpgroup works while the other tile's two MMAs run.
+      // A thread that waits on shared memory after its own tcgen05.commit
+      // stalls until the tensor pipe drains, so the waits are gathered into
+      // the two points a step needs (before each tile's P V MMA) and the
+      // commits follow the MMAs they cover.
       constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);  // bf16 Q, K
       constexpr uint32_t idO = idesc_f32acc(false, 128, D, false, true);    // fp16 P, V
-      const uint32_t qbase = smem_addr(sQ) + t * C::kTileBytes;
+      const uint32_t sQ_addr = smem_addr(sQ);
       const uint32_t sKV_addr = smem_addr(sKV);
-      const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
-      const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
-      uint32_t p_phase = 0, turn_phase = 0;
-      bool first_group = true;
+      uint32_t p_phase[2] = {0, 0};
       uint32_t kvb = 0;
       int uc = 0;
       for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
         int bh, mb;
         unit_coords(p, kCausal, u, bh, mb);
-        const int n_t = kv_tiles(p, kCausal, mb, t);
+        const int n0 = kv_tiles(p, kCausal, mb, 0);
         const int n1 = kv_tiles(p, kCausal, mb, 1);
 #pragma unroll 1
         for (int j = 0; j <= n1; ++j) {
-          if (!(t == 0 && first_group)) {
-            if (!mbar_wait(&sb.turn[t], turn_phase, abort_flag)) {
-              raise_abort(sb, p.err, kDevErrTimeout);
-              goto mma_exit;
-            }
-            turn_phase ^= 1;
-          }
-          first_group = false;
-          const bool do_pv = j >= 1 && j <= n_t;
-          const bool do_s = j < n_t;
           const uint32_t kidx = kvb + 2 * j, vidx = kidx - 1;  // K_j and V_{j-1}
           const uint32_t ks = kidx % C::kStages, vs = vidx % C::kStages;
-          if (do_pv) {
-            // O_t (+)= P_t V_{j-1}, once the softmax has written P_t (and
-            // rescaled O_t), V_{j-1} is in fp16, and the previous unit's
-            // epilogue has drained O_t.
-            if ((j == 1 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
-                !mbar_wait(&sb.p_full[t], p_phase, abort_flag) ||
-                !mbar_wait(&sb.v_ready[vs], (vidx / C::kStages) & 1, abort_flag)) {
-              raise_abort(sb, p.err, kDevErrTimeout);
-              goto mma_exit;
-            }
-            p_phase ^= 1;
-            tc_fence_after_sync();
-            const uint32_t vbase = sKV_addr + vs * C::kTileBytes;
+          bool k_ready = false, v_ready = false;
+          // Unrolled, so the per-tile phases stay in registers: a local-memory
+          // access after a commit would stall this thread until the pipe drains.
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::kChunkBytes, 1024),
-                           idO, (j > 1 || kk > 0) ? 1u : 0u);
-          }
-          if (do_s) {
-            // S_t = Q_t K_j^T
-            if ((j == 0 && !mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) ||
-                !mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag)) {
-              raise_abort(sb, p.err, kDevErrTimeout);
-              goto mma_exit;
+          for (int t = 0; t < 2; ++t) {
+            const int n_t = t ? n1 : n0;
+            const bool do_pv = j >= 1 && j <= n_t;
+            const bool do_s = j < n_t;
+            const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
+            const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
+            // Every wait of this tile's group, in one place.
+            if (do_pv) {
+              if ((j == 1 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
+                  !mbar_wait(&sb.p_full[t], p_phase[t], abort_flag) ||
+                  (!v_ready && !mbar_wait(&sb.v_ready[vs], (vidx / C::kStages) & 1, abort_flag))) {
+                raise_abort(sb, p.err, kDevErrTimeout);
+                goto mma_exit;
+              }
+              p_phase[t] ^= 1;
+              v_ready = true;
+            }
+            if (do_s) {
+              if ((j == 0 && !mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) ||
+                  (!k_ready && !mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag))) {
+                raise_abort(sb, p.err, kDevErrTimeout);
+                goto mma_exit;
+              }
+              k_ready = true;
             }
             tc_fence_after_sync();
-            const uint32_t kbase = sKV_addr + ks * C::kTileBytes;
+            if (do_pv) {
+              // O_t (+)= P_t V_{j-1}
+              const uint32_t vbase = sKV_addr + vs * C::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-              umma_bf16_ss(tS, sdesc_sw128(qbase + off, 16, 1024),
-                           sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 8; ++kk)
+                umma_bf16_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::kChunkBytes, 1024),
+                             idO, (j > 1 || kk > 0) ? 1u : 0u);
             }
+            if (do_s) {
+              // S_t = Q_t K_j^T
+              const uint32_t qbase = sQ_addr + t * C::kTileBytes;
+              const uint32_t kbase = sKV_addr + ks * C::kTileBytes;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                umma_bf16_ss(tS, sdesc_sw128(qbase + off, 16, 1024),
+                             sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&sb.s_full[t]);
+            }
+            if (do_pv && j == n_t) umma_commit(&sb.o_full[t]);
           }
-          mbar_arrive(&sb.turn[1 - t]);  // the other tile's thread may issue now
-          if (do_s) {
-            umma_commit(&sb.s_full[t]);
-            if (j == n_t - 1) umma_commit(&sb.q_empty);
-          }
-          if (do_pv && j == n_t) umma_commit(&sb.o_full[t]);
-          if (j >= 1) umma_commit(&sb.kv_empty[vs]);  // this tile is done with V_{j-1}
-          if (j < n1) umma_commit(&sb.kv_empty[ks]);  // ... and with K_j
+          if (j < n1) umma_commit(&sb.kv_empty[ks]);   // both tiles are done with K_j
+          if (j >= 1) umma_commit(&sb.kv_empty[vs]);   // ... and with V_{j-1}
+          if (j == n1 - 1) umma_commit(&sb.q_empty);   // and with both Q tiles
         }
         kvb += 2 * n1;
       }
     mma_exit:
       // every MMA this thread issued must finish before the TMEM is freed
-      umma_commit(&sb.mma_done[t]);
+      umma_commit(&sb.mma_done[0]);
       {
         int never = 0;
-        mbar_wait(&sb.mma_done[t], 0, &never);
+        mbar_wait(&sb.mma_done[0], 0, &never);
       }
     } else if (warp == 14 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
