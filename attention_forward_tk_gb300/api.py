@@ -34,6 +34,7 @@ EXPORTED = (
     "tk_attn_status_string",
     "tk_attn_version",
     "tk_attn_last_device_error",
+    "tk_attn_debug_drop_load",
 )
 
 
@@ -74,6 +75,8 @@ def library() -> ctypes.CDLL:
         lib.tk_attn_version.argtypes = []
         lib.tk_attn_last_device_error.restype = i
         lib.tk_attn_last_device_error.argtypes = [vp]
+        lib.tk_attn_debug_drop_load.restype = None
+        lib.tk_attn_debug_drop_load.argtypes = [i]
         _lib = lib
         return _lib
 
@@ -103,6 +106,10 @@ def tk_attn_version() -> int:
 
 def tk_attn_last_device_error(stream: int) -> int:
     return int(library().tk_attn_last_device_error(stream))
+
+
+def tk_attn_debug_drop_load(enable: int) -> None:
+    library().tk_attn_debug_drop_load(int(enable))
 
 
 # short aliases

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <functional>
+#include <atomic>
 #include <mutex>
 
 #include "tk_attn.h"
@@ -34,6 +35,7 @@ struct DeviceState {
 };
 
 DeviceState g_dev[kMaxDevices];
+std::atomic<int> g_test_drop_load{0};
 std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 
@@ -183,6 +185,7 @@ extern "C" int tk_attn_fwd(const void *q, const void *k, const void *v, void *o,
   p.num_mblocks = (N + 255) / 256;
   p.num_units = BH * p.num_mblocks;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.test_drop_load = g_test_drop_load.load(std::memory_order_relaxed);
   const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -227,4 +230,8 @@ extern "C" int tk_attn_last_device_error(tk_attn_stream_t stream) {
     return TK_ATTN_ERR_DEVICE_TIMEOUT;
   }
   return TK_ATTN_OK;
+}
+
+extern "C" void tk_attn_debug_drop_load(int enable) {
+  g_test_drop_load.store(enable ? 1 : 0, std::memory_order_relaxed);
 }

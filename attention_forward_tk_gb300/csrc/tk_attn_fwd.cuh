@@ -67,6 +67,7 @@ struct FwdParams {
   int num_mblocks;   // ceil(N / 256)
   int num_units;     // BH * num_mblocks
   float scale_log2;  // scale * log2(e)
+  int test_drop_load;  // test hook: CTA 0 skips its first K load (0 = off)
 };
 
 template <int D>
@@ -100,7 +101,7 @@ struct FwdShared {
   uint64_t v_ready[8];    // V tile converted to fp16           (4 converter warps)
   uint64_t s_full[2];     // S_t = Q_t K^T complete             (commit)
   uint64_t p_full[2];     // P_t in TMEM, O_t rescaled          (4 softmax warps)
-  uint64_t fin_full[2];   // final m, l of a unit in shared     (4 softmax warps)
+  uint64_t fin_full[2][2]; // [unit parity][tile] final m, l in shared (4 softmax warps)
   uint64_t o_full[2];     // last P_t V MMA of a unit done      (commit)
   uint64_t o_free[2];     // epilogue has read O_t              (4 converter warps)
   uint64_t conv_bar;      // converter warps' tile-max exchange (4 converter warps)
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.q_full[t], 1);
       mbar_init(&sb.s_full[t], 1);
       mbar_init(&sb.p_full[t], 4);
-      mbar_init(&sb.fin_full[t], 4);
+      mbar_init(&sb.fin_full[0][t], 4);
+      mbar_init(&sb.fin_full[1][t], 4);
       mbar_init(&sb.o_full[t], 1);
       mbar_init(&sb.o_free[t], 4);
       mbar_init(&sb.mma_done[t], 1);
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&sb.p_full[t]);
-          if (j == n_t - 1) mbar_arrive(&sb.fin_full[t]);
+          if (j == n_t - 1) mbar_arrive(&sb.fin_full[uc & 1][t]);
         }
       }
       kvb += 2 * n1;
@@ -357,7 +359,9 @@ __global__ void __launch_bounds__(512, 1)
         if (pend_bh >= 0 && (j == 1 || !have_unit)) {
 #pragma unroll 1
           for (int t = 0; t < 2; ++t) {
-            if (!mbar_wait(&sb.fin_full[t], pend_uc & 1, abort_flag) ||
+            // fin_full is double-buffered by unit parity: a unit whose tile 0
+            // takes a single K/V step can finish before this epilogue starts.
+            if (!mbar_wait(&sb.fin_full[pend_uc & 1][t], (pend_uc >> 1) & 1, abort_flag) ||
                 !mbar_wait(&sb.o_full[t], pend_uc & 1, abort_flag)) {
               raise_abort(sb, p.err, kDevErrTimeout);
               goto done;
@@ -593,6 +597,12 @@ __global__ void __launch_bounds__(512, 1)
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t s = kv_idx % C::kStages;
             const uint32_t fill = kv_idx / C::kStages;
+            if (p.test_drop_load && blockIdx.x == 0 && uc == 0 && j == 0 && kv == 0) {
+              // Test hook: this load is never issued, so the MMA thread's
+              // bounded wait for it runs out and the kernel reports a timeout.
+              ++kv_idx;
+              continue;
+            }
             if (fill > 0 && !mbar_wait(&sb.kv_empty[s], (fill - 1) & 1, abort_flag)) {
               raise_abort(sb, p.err, kDevErrTimeout);
               goto load_exit;
@@ -612,6 +622,7 @@ __global__ void __launch_bounds__(512, 1)
         int never = 0;
         for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_idx; ++s) {
           const uint32_t last = kv_idx - 1 - ((kv_idx - 1 - s) % C::kStages);
+          if (p.test_drop_load && blockIdx.x == 0 && last == 0) continue;  // never issued
           mbar_wait(&sb.kv_full[s], (last / C::kStages) & 1, &never);
         }
         if (q_loads > 0) {

@@ -105,6 +105,17 @@ int tk_attn_version(void);
  */
 int tk_attn_last_device_error(tk_attn_stream_t stream);
 
+/*
+ * tk_attn_debug_drop_load -- test hook for the device-side failure path.
+ * While enabled (nonzero), every tk_attn_fwd launch skips one K/V load in its
+ * first CTA; the MMA thread's bounded wait for that load runs out after about
+ * a second, the kernel abandons its work (outputs incomplete) and
+ * tk_attn_last_device_error then returns TK_ATTN_ERR_DEVICE_TIMEOUT.  Nothing
+ * faults or hangs and the CUDA context stays usable.  Process-wide; off by
+ * default.  Not part of the attention operation.
+ */
+void tk_attn_debug_drop_load(int enable);
+
 #ifdef __cplusplus
 }
 #endif
