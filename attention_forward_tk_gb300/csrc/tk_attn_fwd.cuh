@@ -322,6 +322,16 @@ __global__ void __launch_bounds__(512, 1)
           sb.m_fin[uc & 1][t][row] = m_run;
           sb.l_fin[uc & 1][t][row] = l_run;
         }
+        // The MMA thread's next group for this tile is [P_t V_j, S_t = Q_t K_{j+1}^T]
+        // and it waits only for this signal: make sure K_{j+1} has landed
+        // (V_j is converted: waited above).
+        if (j + 1 < n_t) {
+          const uint32_t kidx = kvb + 2 * (j + 1);
+          if (!mbar_wait(&sb.kv_full[kidx % C::kStages], (kidx / C::kStages) & 1, abort_flag)) {
+            raise_abort(sb, p.err, kDevErrTimeout);
+            goto done;
+          }
+        }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
@@ -506,7 +516,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int j = 0; j <= n1; ++j) {
           const uint32_t kidx = kvb + 2 * j, vidx = kidx - 1;  // K_j and V_{j-1}
           const uint32_t ks = kidx % C::kStages, vs = vidx % C::kStages;
-          bool k_ready = false, v_ready = false;
+          bool k_ready = false;
           // Unrolled, so the per-tile phases stay in registers: a local-memory
           // access after a commit would stall this thread until the pipe drains.
 #pragma unroll
@@ -516,18 +526,18 @@ __global__ void __launch_bounds__(512, 1)
             const bool do_s = j < n_t;
             const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
             const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
-            // Every wait of this tile's group, in one place.
+            // One wait per group on the steady path: the softmax signals P_t
+            // only after V_{j-1} is converted and K_j has landed (see there).
+            // The first S of a unit waits for its Q tile and K_0 here.
             if (do_pv) {
               if ((j == 1 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
-                  !mbar_wait(&sb.p_full[t], p_phase[t], abort_flag) ||
-                  (!v_ready && !mbar_wait(&sb.v_ready[vs], (vidx / C::kStages) & 1, abort_flag))) {
+                  !mbar_wait(&sb.p_full[t], p_phase[t], abort_flag)) {
                 raise_abort(sb, p.err, kDevErrTimeout);
                 goto mma_exit;
               }
               p_phase[t] ^= 1;
-              v_ready = true;
             }
-            if (do_s) {
+            if (do_s && (j == 0 || !do_pv)) {
               if ((j == 0 && !mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) ||
                   (!k_ready && !mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag))) {
                 raise_abort(sb, p.err, kDevErrTimeout);
