@@ -186,6 +186,16 @@ extern "C" int tk_attn_fwd(const void *q, const void *k, const void *v, void *o,
   p.num_units = BH * p.num_mblocks;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.test_drop_load = g_test_drop_load.load(std::memory_order_relaxed);
+  // Causal order: sections of heads whose K and V (4*N*D bytes each head)
+  // take about 64 MB together, half the L2, so concurrent query blocks of a
+  // section reuse K/V from L2 instead of re-reading HBM.
+  {
+    const long long per_head = 4LL * N * D;
+    long long g = (64LL << 20) / (per_head > 0 ? per_head : 1);
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    p.head_group = (int)g;
+  }
   const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -68,6 +68,7 @@ struct FwdParams {
   int num_units;     // BH * num_mblocks
   float scale_log2;  // scale * log2(e)
   int test_drop_load;  // test hook: CTA 0 skips its first K load (0 = off)
+  int head_group;      // causal unit order: heads per section (>= 1)
 };
 
 template <int D>
@@ -120,12 +121,18 @@ __device__ __forceinline__ void raise_abort(FwdShared &sb, int *err, int code) {
 }
 
 // Unit u -> (bh, mblock).  Non-causal: head-major, so CTAs running at the same
-// time share a head's K/V in L2.  Causal: longest query blocks first.
+// time share a head's K/V in L2.  Causal: heads are taken in sections of
+// head_group (sized on the host so a section's K/V fits in L2), and within a
+// section the longest query blocks come first.
 __device__ __forceinline__ void unit_coords(const FwdParams &p, bool causal, int u, int &bh,
                                             int &mb) {
   if (causal) {
-    mb = p.num_mblocks - 1 - u / p.BH;
-    bh = u % p.BH;
+    const int per_section = p.head_group * p.num_mblocks;
+    const int section = u / per_section;
+    const int r = u - section * per_section;
+    const int g = min(p.head_group, p.BH - section * p.head_group);  // heads in this section
+    mb = p.num_mblocks - 1 - r / g;
+    bh = section * p.head_group + r % g;
   } else {
     bh = u / p.num_mblocks;
     mb = u % p.num_mblocks;
