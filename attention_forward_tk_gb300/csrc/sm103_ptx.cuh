@@ -379,6 +379,31 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// max(|a|, |b|) per f16 lane (the sign bit of the result is the xor of the
+// inputs' signs; callers mask it).
+__device__ __forceinline__ uint32_t maxabs_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Eight bf16 values (four packed words) -> eight f16 values, round to nearest.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                    bf16x2_to_f16x2(v.w));
+}
+// The same, each value multiplied by `sc` (a power of two) first.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t v, float sc) {
+  return pack_f16x2(__uint_as_float(v << 16) * sc, __uint_as_float(v & 0xffff0000u) * sc);
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v, float sc) {
+  return make_uint4(bf16x2_to_f16x2_scaled(v.x, sc), bf16x2_to_f16x2_scaled(v.y, sc),
+                    bf16x2_to_f16x2_scaled(v.z, sc), bf16x2_to_f16x2_scaled(v.w, sc));
+}
+
 // Non-blocking probe of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
   uint32_t done;

@@ -261,17 +261,6 @@ __global__ void __launch_bounds__(512, 1)
         const bool grow = m_cand > m_run + kTau;
         const float m_new = grow ? m_cand : m_run;
         const float fac = grow ? ex2_approx(m_run - m_new) : 1.0f;  // 0 on the first tile
-        // Exponent of the V tile this step multiplies (set by the converter).
-        const uint32_t vidx = kvb + 2 * j + 1;
-        if (!mbar_wait(&sb.v_ready[vidx % C::kStages], (vidx / C::kStages) & 1, abort_flag)) {
-          raise_abort(sb, p.err, kDevErrTimeout);
-          goto done;
-        }
-        const int e_j = sb.v_exp[vidx % C::kStages];
-        // O_t must be multiplied by this factor before the P_t V MMA of this
-        // step: the reference max moved, or V_j was scaled by a smaller 2^e.
-        const float ofac = (e_j == e_cur) ? fac : fac * exp2i(e_j - e_cur);
-        e_cur = e_j;
         m_run = m_new;
         // P = 2^(s*c - m_run) <= 2^kTau, rounded to fp16 for the P V MMA;
         // the row sum is taken over the fp32 P.
@@ -297,6 +286,18 @@ __global__ void __launch_bounds__(512, 1)
         }
         tmem_st_32x32b_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
         tmem_st_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        // Exponent of the V tile this step multiplies (set by the converter;
+        // waited here, after the P stores, to keep it off the exp path).
+        const uint32_t vidx = kvb + 2 * j + 1;
+        if (!mbar_wait(&sb.v_ready[vidx % C::kStages], (vidx / C::kStages) & 1, abort_flag)) {
+          raise_abort(sb, p.err, kDevErrTimeout);
+          goto done;
+        }
+        const int e_j = sb.v_exp[vidx % C::kStages];
+        // O_t must be multiplied by this factor before the P_t V MMA of this
+        // step: the reference max moved, or V_j was scaled by a smaller 2^e.
+        const float ofac = (e_j == e_cur) ? fac : fac * exp2i(e_j - e_cur);
+        e_cur = e_j;
         // Rescale this warp's O rows (after the scores are dead, to keep
         // register pressure down).  S_t of this step is complete, and its
         // commit covers the previous P_t V MMA: O_t holds its accumulated value.
@@ -429,58 +430,74 @@ __global__ void __launch_bounds__(512, 1)
         }
         uint4 *tile = reinterpret_cast<uint4 *>(sKV + st * C::kTileBytes);
         uint4 w[C::kConvVec];
-        uint32_t amax2 = 0;  // per-16-bit-lane max of |bf16| bit patterns
 #pragma unroll
-        for (int i = 0; i < C::kConvVec; ++i) {
-          w[i] = tile[ct + 128 * i];
-          amax2 = max_u16x2(amax2, w[i].x & 0x7fff7fffu);
-          amax2 = max_u16x2(amax2, w[i].y & 0x7fff7fffu);
-          amax2 = max_u16x2(amax2, w[i].z & 0x7fff7fffu);
-          amax2 = max_u16x2(amax2, w[i].w & 0x7fff7fffu);
-        }
-        const uint32_t wmax =
-            __reduce_max_sync(0xffffffffu, max(amax2 & 0xffffu, amax2 >> 16));
-        if (lane == 0) {
-          sb.conv_max[conv_count & 1][cw] = wmax;
-          mbar_arrive(&sb.conv_bar);
-        }
-        if (!mbar_wait(&sb.conv_bar, conv_count & 1, abort_flag)) {
-          raise_abort(sb, p.err, kDevErrTimeout);
-          goto done;
-        }
-        const uint32_t amax = max(max(sb.conv_max[conv_count & 1][0], sb.conv_max[conv_count & 1][1]),
-                                  max(sb.conv_max[conv_count & 1][2], sb.conv_max[conv_count & 1][3]));
-        ++conv_count;
-        // |v| < 2^(k+1) with k = biased exponent - 127.  fp16 holds every
-        // bf16 value below 2^16 exactly; scale larger tiles down by 2^(15-k).
-        // Non-finite inputs (exponent field 255) are passed through unscaled.
-        const int kexp = (int)(amax >> 7) - 127;
-        if (amax < 0x7f80u && kexp >= 16) e_run = min(e_run, 15 - kexp);
+        for (int i = 0; i < C::kConvVec; ++i) w[i] = tile[ct + 128 * i];
+        // Convert at the unit's current exponent and store; fp16 holds every
+        // bf16 value below 2^16 exactly, and a value at or above it becomes
+        // inf, which the running |max| below detects.
+        uint32_t hmax = 0;  // per-16-bit-lane max |fp16| of the results
         if (e_run == 0) {
 #pragma unroll
           for (int i = 0; i < C::kConvVec; ++i) {
-            uint4 o;
-            o.x = pack_f16x2(__uint_as_float(w[i].x << 16), __uint_as_float(w[i].x & 0xffff0000u));
-            o.y = pack_f16x2(__uint_as_float(w[i].y << 16), __uint_as_float(w[i].y & 0xffff0000u));
-            o.z = pack_f16x2(__uint_as_float(w[i].z << 16), __uint_as_float(w[i].z & 0xffff0000u));
-            o.w = pack_f16x2(__uint_as_float(w[i].w << 16), __uint_as_float(w[i].w & 0xffff0000u));
+            const uint4 o = bf16x8_to_f16x8(w[i]);
+            hmax = maxabs_f16x2(hmax, maxabs_f16x2(maxabs_f16x2(o.x, o.y), maxabs_f16x2(o.z, o.w)));
             tile[ct + 128 * i] = o;
           }
         } else {
           const float sc = exp2i(e_run);
 #pragma unroll
           for (int i = 0; i < C::kConvVec; ++i) {
-            uint4 o;
-            o.x = pack_f16x2(__uint_as_float(w[i].x << 16) * sc,
-                             __uint_as_float(w[i].x & 0xffff0000u) * sc);
-            o.y = pack_f16x2(__uint_as_float(w[i].y << 16) * sc,
-                             __uint_as_float(w[i].y & 0xffff0000u) * sc);
-            o.z = pack_f16x2(__uint_as_float(w[i].z << 16) * sc,
-                             __uint_as_float(w[i].z & 0xffff0000u) * sc);
-            o.w = pack_f16x2(__uint_as_float(w[i].w << 16) * sc,
-                             __uint_as_float(w[i].w & 0xffff0000u) * sc);
+            const uint4 o = bf16x8_to_f16x8_scaled(w[i], sc);
+            hmax = maxabs_f16x2(hmax, maxabs_f16x2(maxabs_f16x2(o.x, o.y), maxabs_f16x2(o.z, o.w)));
             tile[ct + 128 * i] = o;
           }
+        }
+        const bool ovf = __any_sync(0xffffffffu, ((hmax & 0x7fffu) >= 0x7c00u) ||
+                                                     (((hmax >> 16) & 0x7fffu) >= 0x7c00u));
+        // All four converter warps must agree before the tile is released.
+        if (lane == 0) {
+          sb.conv_max[conv_count & 1][cw] = ovf ? 1u : 0u;
+          mbar_arrive(&sb.conv_bar);
+        }
+        if (!mbar_wait(&sb.conv_bar, conv_count & 1, abort_flag)) {
+          raise_abort(sb, p.err, kDevErrTimeout);
+          goto done;
+        }
+        const bool any_ovf = (sb.conv_max[conv_count & 1][0] | sb.conv_max[conv_count & 1][1] |
+                              sb.conv_max[conv_count & 1][2] | sb.conv_max[conv_count & 1][3]) != 0;
+        ++conv_count;
+        if (any_ovf) {
+          // Rare: magnitudes at or above 2^16 * 2^-e_run.  Find the tile's
+          // largest |v| (bf16 bit patterns order like magnitudes), lower the
+          // unit's exponent so it fits, and convert again.
+          uint32_t amax2 = 0;
+#pragma unroll
+          for (int i = 0; i < C::kConvVec; ++i) {
+            amax2 = max_u16x2(amax2, w[i].x & 0x7fff7fffu);
+            amax2 = max_u16x2(amax2, w[i].y & 0x7fff7fffu);
+            amax2 = max_u16x2(amax2, w[i].z & 0x7fff7fffu);
+            amax2 = max_u16x2(amax2, w[i].w & 0x7fff7fffu);
+          }
+          const uint32_t wmax = __reduce_max_sync(0xffffffffu, max(amax2 & 0xffffu, amax2 >> 16));
+          if (lane == 0) {
+            sb.conv_max[conv_count & 1][cw] = wmax;
+            mbar_arrive(&sb.conv_bar);
+          }
+          if (!mbar_wait(&sb.conv_bar, conv_count & 1, abort_flag)) {
+            raise_abort(sb, p.err, kDevErrTimeout);
+            goto done;
+          }
+          const uint32_t amax =
+              max(max(sb.conv_max[conv_count & 1][0], sb.conv_max[conv_count & 1][1]),
+                  max(sb.conv_max[conv_count & 1][2], sb.conv_max[conv_count & 1][3]));
+          ++conv_count;
+          // |v| < 2^(k+1) with k = biased exponent - 127; scale by 2^(15-k).
+          // Non-finite inputs (exponent field 255) are passed through.
+          const int kexp = (int)(amax >> 7) - 127;
+          if (amax < 0x7f80u && kexp >= 16) e_run = min(e_run, 15 - kexp);
+          const float sc = exp2i(e_run);
+#pragma unroll
+          for (int i = 0; i < C::kConvVec; ++i) tile[ct + 128 * i] = bf16x8_to_f16x8_scaled(w[i], sc);
         }
         fence_proxy_async_smem();  // the generic writes become visible to the tensor core
         if (ct == 0) sb.v_exp[st] = e_run;
