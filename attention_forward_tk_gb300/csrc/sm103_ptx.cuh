@@ -245,6 +245,54 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor split in two 32-bit words, for issue loops that step a
+// descriptor by adding byte offsets / 16 to its low word.  The address field
+// holds a shared-memory offset / 16 (< 2^14 for the 228 KB window), so an add
+// that stays inside the window never carries into the leading-offset field.
+__host__ __device__ constexpr uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+// tcgen05.mma kind::f16 from descriptor words; kAcc is the compile-time
+// accumulate flag (0: D = A B, 1: D += A B), so no per-issue predicate setup.
+template <uint32_t kAcc>
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                          uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 a, {%1, %3};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+template <uint32_t kAcc>
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(kAcc)
+      : "memory");
+}
+// Runtime accumulate flag (only where it is not known at compile time).
+__device__ __forceinline__ void umma_ts_w_rt(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                             uint32_t hi, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // Pretend to redefine registers so the compiler cannot move their uses above
 // a preceding tcgen05.wait::ld.
 __device__ __forceinline__ void reg_barrier(uint32_t &r) { asm volatile("" : "+r"(r)); }

@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------ V converter + epilogue
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
     const int cw = warp - 8;                 // converter warp 0..3
     const int ct = threadIdx.x - 256;        // converter thread 0..127
     const int row = (warp & 3) * 32 + lane;  // epilogue: row == TMEM lane
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(512, 1)
       kvb += 2 * n1;
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- MMA issue
       // Step j issues P0 V_{j-1}, S0 = Q0 K_j^T, then P1 V_{j-1}, S1 = Q1 K_j^T,
@@ -526,8 +526,12 @@ __global__ void __launch_bounds__(512, 1)
       // commits follow the MMAs they cover.
       constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);  // bf16 Q, K
       constexpr uint32_t idO = idesc_f32acc(false, 128, D, false, true);    // fp16 P, V
-      const uint32_t sQ_addr = smem_addr(sQ);
-      const uint32_t sKV_addr = smem_addr(sKV);
+      // Descriptor words: the low word carries the address / 16, stepped by
+      // adds; the high word (stride 1024 B, 128-byte swizzle) is shared.
+      const uint32_t dhi = sdesc_sw128_hi(1024);
+      const uint32_t q_lo = sdesc_sw128_lo(smem_addr(sQ), 16);
+      const uint32_t k_lo0 = sdesc_sw128_lo(smem_addr(sKV), 16);
+      const uint32_t v_lo0 = sdesc_sw128_lo(smem_addr(sKV), C::kChunkBytes);
       uint32_t p_phase[2] = {0, 0};
       uint32_t kvb = 0;
       int uc = 0;
@@ -571,22 +575,22 @@ __global__ void __launch_bounds__(512, 1)
             }
             tc_fence_after_sync();
             if (do_pv) {
-              // O_t (+)= P_t V_{j-1}
-              const uint32_t vbase = sKV_addr + vs * C::kTileBytes;
+              // O_t (+)= P_t V_{j-1}: 16 keys (8 P columns, 2048 B of V) per MMA
+              const uint32_t v_lo = v_lo0 + vs * (C::kTileBytes >> 4);
+              umma_ts_w_rt(tO, tS, v_lo, dhi, idO, j > 1 ? 1u : 0u);
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_bf16_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 2048, C::kChunkBytes, 1024),
-                             idO, (j > 1 || kk > 0) ? 1u : 0u);
+              for (int kk = 1; kk < 8; ++kk)
+                umma_ts_w<1>(tO, tS + kk * 8, v_lo + kk * (2048 >> 4), dhi, idO);
             }
             if (do_s) {
-              // S_t = Q_t K_j^T
-              const uint32_t qbase = sQ_addr + t * C::kTileBytes;
-              const uint32_t kbase = sKV_addr + ks * C::kTileBytes;
+              // S_t = Q_t K_j^T: 16 head-dim columns (32 B of a swizzled row) per MMA
+              const uint32_t a_lo = q_lo + t * (C::kTileBytes >> 4);
+              const uint32_t b_lo = k_lo0 + ks * (C::kTileBytes >> 4);
+              umma_ss_w<0>(tS, a_lo, b_lo, dhi, idS);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                umma_bf16_ss(tS, sdesc_sw128(qbase + off, 16, 1024),
-                             sdesc_sw128(kbase + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+              for (int kk = 1; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+                umma_ss_w<1>(tS, a_lo + off, b_lo + off, dhi, idS);
               }
               umma_commit(&sb.s_full[t]);
             }
