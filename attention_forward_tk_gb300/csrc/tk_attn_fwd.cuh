@@ -18,13 +18,14 @@
 //   warps 0-3   softmax for Q tile 0 (thread = query row = TMEM lane)
 //   warps 4-7   softmax for Q tile 1
 //   warps 8-11  V converter (bf16 -> fp16 in shared memory) and epilogue
-//   warp 12     tcgen05 MMA issue (one thread) and TMEM allocation
+//   warp 12     tcgen05 MMA issue for Q tile 0 (one thread), TMEM allocation
+//   warp 13     tcgen05 MMA issue for Q tile 1 (one thread)
 //   warp 14     TMA producer (one thread): Q tiles, then a K/V ring
-//   warps 13,15 idle (keep the register split warpgroup-aligned)
-// The MMA thread issues, per K/V step, P0 V, S0, P1 V, S1: each softmax
-// warpgroup works while the other tile's two MMAs run.  A thread that waits
-// on shared memory after its own tcgen05.commit stalls until the tensor pipe
-// drains, so the MMA thread waits at only the two points a step needs.
+//   warp 15     idle (keeps the register split warpgroup-aligned)
+// Per K/V step each issuing thread runs its tile's P V and S MMAs; while one
+// softmax warpgroup works, the other tile's MMAs run.  The issue slots of an
+// SM sub-partition are shared with two softmax warps, so each tile gets its
+// own issuing thread on its own sub-partition.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [0,128) S0 / P0    [128,256) S1 / P1    [256,256+D) O0    [256+D,256+2D) O1
@@ -85,6 +86,12 @@ struct FwdCfg {
   static constexpr int kThreads = 512;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // With D = 64 the tensor memory has room for P next to S (columns
+  // [384, 512)), so the next S MMA of a tile needs only the softmax to have
+  // read S, not its whole pass: S and P are decoupled.  With D = 128 the 512
+  // columns hold S and O alone and P overwrites S.
+  static constexpr bool kSplitP = D == 64;
+  static constexpr uint32_t kColP0 = kSplitP ? 384 : kColS0, kColP1 = kSplitP ? 448 : kColS1;
   // converter: 16-byte words of one V tile per converter thread
   static constexpr int kConvVec = kTileBytes / 16 / 128;
   static_assert(kStages % 2 == 0, "K tiles in even stages, V tiles in odd stages");
@@ -96,17 +103,19 @@ constexpr float kTau = 8.0f;
 // Shared-memory bookkeeping that is not tile data.
 struct FwdShared {
   uint64_t q_full[2];     // TMA Q tile landed                  (1 + tx)
-  uint64_t q_empty;       // S MMAs of both tiles done with Q   (commit)
+  uint64_t q_empty;       // S MMAs of both tiles done with Q   (commit per issuer)
   uint64_t kv_full[8];    // TMA K or V tile landed             (1 + tx)
-  uint64_t kv_empty[8];   // both tiles' MMAs done with stage   (commit)
+  uint64_t kv_empty[8];   // both tiles' MMAs done with stage   (commit per issuer)
   uint64_t v_ready[8];    // V tile converted to fp16           (4 converter warps)
   uint64_t s_full[2];     // S_t = Q_t K^T complete             (commit)
+  uint64_t s_free[2];     // softmax has read S_t (split P only) (4 softmax warps)
+  uint64_t pv_done[2];    // P_t V MMA complete (split P only)  (commit)
   uint64_t p_full[2];     // P_t in TMEM, O_t rescaled          (4 softmax warps)
   uint64_t fin_full[2][2]; // [unit parity][tile] final m, l in shared (4 softmax warps)
   uint64_t o_full[2];     // last P_t V MMA of a unit done      (commit)
   uint64_t o_free[2];     // epilogue has read O_t              (4 converter warps)
   uint64_t conv_bar;      // converter warps' tile-max exchange (4 converter warps)
-  uint64_t mma_done[2];   // every MMA of the issuing thread done (commit; [0] used)
+  uint64_t mma_done[2];   // every MMA of issuing thread t done   (commit)
   uint32_t tmem_base;
   int abort;
   int v_exp[8];           // power-of-two exponent of each converted V stage
@@ -147,6 +156,26 @@ __device__ __forceinline__ int kv_tiles(const FwdParams &p, bool causal, int mb,
   return last_row / 128 + 1;
 }
 
+// S = Q K^T for one Q tile: 16 head-dim columns (32 B of a swizzled row) per MMA.
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tS, uint32_t a_lo, uint32_t b_lo, uint32_t dhi,
+                                        uint32_t idS) {
+  umma_ss_w<0>(tS, a_lo, b_lo, dhi, idS);
+#pragma unroll
+  for (int kk = 1; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * FwdCfg<D>::kChunkBytes + (kk & 3) * 32) >> 4;
+    umma_ss_w<1>(tS, a_lo + off, b_lo + off, dhi, idS);
+  }
+}
+
+// O (+)= P V for one Q tile: 16 keys (8 P columns, 2048 B of V) per MMA.
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, uint32_t dhi,
+                                         uint32_t idO, uint32_t acc) {
+  umma_ts_w_rt(tO, tP, v_lo, dhi, idO, acc);
+#pragma unroll
+  for (int kk = 1; kk < 8; ++kk) umma_ts_w<1>(tO, tP + kk * 8, v_lo + kk * (2048 >> 4), dhi, idO);
+}
+
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(512, 1)
     tk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -168,6 +197,8 @@ __global__ void __launch_bounds__(512, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sb.q_full[t], 1);
       mbar_init(&sb.s_full[t], 1);
+      mbar_init(&sb.s_free[t], 4);
+      mbar_init(&sb.pv_done[t], 1);
       mbar_init(&sb.p_full[t], 4);
       mbar_init(&sb.fin_full[0][t], 4);
       mbar_init(&sb.fin_full[1][t], 4);
@@ -175,10 +206,10 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.o_free[t], 4);
       mbar_init(&sb.mma_done[t], 1);
     }
-    mbar_init(&sb.q_empty, 1);
+    mbar_init(&sb.q_empty, C::kSplitP ? 2 : 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sb.kv_full[s], 1);
-      mbar_init(&sb.kv_empty[s], 1);
+      mbar_init(&sb.kv_empty[s], C::kSplitP ? 2 : 1);
       mbar_init(&sb.v_ready[s], 4);
     }
     mbar_init(&sb.conv_bar, 4);
@@ -207,8 +238,10 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
+    const uint32_t tP = tmem + lane_off + (t ? C::kColP1 : C::kColP0);
     const float c = p.scale_log2;
     uint32_t s_phase = 0;
+    uint32_t steps = 0;  // S tiles this warp has processed (all units): P V MMAs issued before
     uint32_t kvb = 0;  // K/V load index of this unit's K_0
     int uc = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
@@ -234,6 +267,12 @@ __global__ void __launch_bounds__(512, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 128; ++i) reg_barrier(s[i]);
+        if constexpr (C::kSplitP) {
+          // S_t is in registers: the MMA thread may overwrite it with the next S.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sb.s_free[t]);
+        }
         // Mask keys beyond N, and keys after the query under the causal mask.
         const int k0 = j * 128;
         const bool need_mask = (k0 + 128 > p.N) || (kCausal && k0 + 127 > mb * 256 + t * 128);
@@ -284,8 +323,18 @@ __global__ void __launch_bounds__(512, 1)
           la = f2_add(la, f2_pack(p0, p1));
           lb = f2_add(lb, f2_pack(p2, p3));
         }
-        tmem_st_32x32b_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if constexpr (C::kSplitP) {
+          // The previous P_t V MMA must be done reading P_t (and writing O_t,
+          // which the rescale below touches).
+          if (steps > 0 && !mbar_wait(&sb.pv_done[t], (steps - 1) & 1, abort_flag)) {
+            raise_abort(sb, p.err, kDevErrTimeout);
+            goto done;
+          }
+          tc_fence_after_sync();
+        }
+        ++steps;
+        tmem_st_32x32b_x32(tP + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st_32x32b_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         // Exponent of the V tile this step multiplies (set by the converter;
         // waited here, after the P stores, to keep it off the exp path).
         const uint32_t vidx = kvb + 2 * j + 1;
@@ -299,8 +348,9 @@ __global__ void __launch_bounds__(512, 1)
         const float ofac = (e_j == e_cur) ? fac : fac * exp2i(e_j - e_cur);
         e_cur = e_j;
         // Rescale this warp's O rows (after the scores are dead, to keep
-        // register pressure down).  S_t of this step is complete, and its
-        // commit covers the previous P_t V MMA: O_t holds its accumulated value.
+        // register pressure down).  The previous P_t V MMA is complete (its
+        // commit is covered by this step's S_t commit, or waited above when
+        // P is split from S): O_t holds its accumulated value.
         if (j > 0 && __any_sync(0xffffffffu, ofac != 1.0f)) {
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -330,10 +380,10 @@ __global__ void __launch_bounds__(512, 1)
           sb.m_fin[uc & 1][t][row] = m_run;
           sb.l_fin[uc & 1][t][row] = l_run;
         }
-        // The MMA thread's next group for this tile is [P_t V_j, S_t = Q_t K_{j+1}^T]
-        // and it waits only for this signal: make sure K_{j+1} has landed
-        // (V_j is converted: waited above).
-        if (j + 1 < n_t) {
+        // Shared S/P: the MMA thread's next group for this tile is
+        // [P_t V_j, S_t = Q_t K_{j+1}^T] and it waits only for this signal:
+        // make sure K_{j+1} has landed (V_j is converted: waited above).
+        if (!C::kSplitP && j + 1 < n_t) {
           const uint32_t kidx = kvb + 2 * (j + 1);
           if (!mbar_wait(&sb.kv_full[kidx % C::kStages], (kidx / C::kStages) & 1, abort_flag)) {
             raise_abort(sb, p.err, kDevErrTimeout);
@@ -516,14 +566,94 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
-    if (warp == 12 && lane == 0) {
+    if constexpr (C::kSplitP) {
+      if ((warp == 12 || warp == 13) && lane == 0) {
+        // ---------------------------------------------------------- MMA issue
+        // Split P (D = 64): one issuing thread per Q tile (warp 12: tile 0,
+        // warp 13: tile 1), on two SM sub-partitions whose issue slots the
+        // softmax warps contend for; each tile's MMAs touch only its own tensor
+        // memory, and K/V stages and Q buffers are released by one commit from
+        // each thread.  Step j issues S_t for K_j as soon as the softmax has read
+        // the previous S_t, then P_t V_{j-1} when the softmax pass ends, so the
+        // next scores are computed while the softmax of the current ones runs.
+        const int t = warp - 12;
+        constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);  // bf16 Q, K
+        constexpr uint32_t idO = idesc_f32acc(false, 128, D, false, true);    // fp16 P, V
+        // Descriptor words: the low word carries the address / 16, stepped by
+        // adds; the high word (stride 1024 B, 128-byte swizzle) is shared.
+        const uint32_t dhi = sdesc_sw128_hi(1024);
+        const uint32_t a_lo = sdesc_sw128_lo(smem_addr(sQ), 16) + t * (C::kTileBytes >> 4);
+        const uint32_t k_lo0 = sdesc_sw128_lo(smem_addr(sKV), 16);
+        const uint32_t v_lo0 = sdesc_sw128_lo(smem_addr(sKV), C::kChunkBytes);
+        const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
+        const uint32_t tP = tmem + (t ? C::kColP1 : C::kColP0);
+        const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
+        uint32_t p_phase = 0;
+        uint32_t s_cnt = 0;  // S MMAs issued (split P: s_free phases)
+        uint32_t kvb = 0;
+        int uc = 0;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+          int bh, mb;
+          unit_coords(p, kCausal, u, bh, mb);
+          const int n1 = kv_tiles(p, kCausal, mb, 1);
+          const int n_t = t ? n1 : kv_tiles(p, kCausal, mb, 0);
+  #pragma unroll 1
+          for (int j = 0; j <= n1; ++j) {
+            const uint32_t kidx = kvb + 2 * j, vidx = kidx - 1;  // K_j and V_{j-1}
+            const uint32_t ks = kidx % C::kStages, vs = vidx % C::kStages;
+            const bool do_s = j < n_t, do_pv = j >= 1 && j <= n_t;
+            if (do_s) {
+              // S_t = Q_t K_j^T once K_j has landed and the softmax has read
+              // the previous S_t
+              if (!mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag) ||
+                  (j == 0 && !mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) ||
+                  (s_cnt > 0 && !mbar_wait(&sb.s_free[t], (s_cnt - 1) & 1, abort_flag))) {
+                raise_abort(sb, p.err, kDevErrTimeout);
+                goto mma_exit_split;
+              }
+              ++s_cnt;
+              tc_fence_after_sync();
+              issue_s<D>(tS, a_lo, k_lo0 + ks * (C::kTileBytes >> 4), dhi, idS);
+              umma_commit(&sb.s_full[t]);
+            }
+            if (do_pv) {
+              // O_t (+)= P_t V_{j-1} once the softmax has written P_t
+              if ((j == 1 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
+                  !mbar_wait(&sb.p_full[t], p_phase, abort_flag)) {
+                raise_abort(sb, p.err, kDevErrTimeout);
+                goto mma_exit_split;
+              }
+              p_phase ^= 1;
+              tc_fence_after_sync();
+              issue_pv(tO, tP, v_lo0 + vs * (C::kTileBytes >> 4), dhi, idO, j > 1 ? 1u : 0u);
+              umma_commit(&sb.pv_done[t]);
+              if (j == n_t) umma_commit(&sb.o_full[t]);
+            }
+            // this tile is done with K_j, V_{j-1} (and, after the unit's last S,
+            // with its Q tile); every stage gets one commit from each thread
+            if (j < n1) umma_commit(&sb.kv_empty[ks]);
+            if (j >= 1) umma_commit(&sb.kv_empty[vs]);
+            if (j == n1 - 1) umma_commit(&sb.q_empty);
+          }
+          kvb += 2 * n1;
+        }
+      mma_exit_split:
+        // every MMA this thread issued must finish before the TMEM is freed
+        umma_commit(&sb.mma_done[t]);
+        {
+          int never = 0;
+          mbar_wait(&sb.mma_done[t], 0, &never);
+        }
+      }
+    } else if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- MMA issue
-      // Step j issues P0 V_{j-1}, S0 = Q0 K_j^T, then P1 V_{j-1}, S1 = Q1 K_j^T,
-      // so each softmax warpgroup works while the other tile's two MMAs run.
-      // A thread that waits on shared memory after its own tcgen05.commit
-      // stalls until the tensor pipe drains, so the waits are gathered into
-      // the two points a step needs (before each tile's P V MMA) and the
-      // commits follow the MMAs they cover.
+      // Shared S/P (D = 128): one issuing thread.  Step j issues P0 V_{j-1},
+      // S0 = Q0 K_j^T, then P1 V_{j-1}, S1 = Q1 K_j^T, so each softmax
+      // warpgroup works while the other tile's two MMAs run, and a tile's
+      // scores complete as one group (two independent issuers would
+      // interleave the tiles' MMAs and delay both).  One wait per tile and
+      // step: the softmax signals P_t only once V_{j-1} is converted and K_j
+      // has landed.
       constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);  // bf16 Q, K
       constexpr uint32_t idO = idesc_f32acc(false, 128, D, false, true);    // fp16 P, V
       // Descriptor words: the low word carries the address / 16, stepped by
@@ -609,7 +739,9 @@ __global__ void __launch_bounds__(512, 1)
         int never = 0;
         mbar_wait(&sb.mma_done[0], 0, &never);
       }
-    } else if (warp == 14 && lane == 0) {
+
+    }
+    if (warp == 14 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       uint32_t kv_idx = 0;
       uint32_t q_loads = 0;  // Q tile pairs issued
