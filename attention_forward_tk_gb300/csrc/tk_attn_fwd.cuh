@@ -81,7 +81,10 @@ struct FwdCfg {
   static constexpr int kChunks = D / 64;           // 128-byte swizzle column chunks
   static constexpr int kChunkBytes = kBM * 128;    // one chunk: 128 rows x 128 B
   static constexpr int kStages = D == 128 ? 4 : 8; // K/V ring depth (tiles; even)
-  static constexpr int kSmemBytes = (2 + kStages) * kTileBytes;
+  // Q tile pairs in shared memory: with D = 64 the next unit's pair loads
+  // while the current one is in use; with D = 128 there is room for one.
+  static constexpr int kQBufs = D == 64 ? 2 : 1;
+  static constexpr int kSmemBytes = (2 * kQBufs + kStages) * kTileBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
   static constexpr int kThreads = 512;
   static constexpr uint32_t kTmemCols = 512;
@@ -102,14 +105,12 @@ constexpr float kTau = 8.0f;
 
 // Shared-memory bookkeeping that is not tile data.
 struct FwdShared {
-  uint64_t q_full[2];     // TMA Q tile landed                  (1 + tx)
-  uint64_t q_empty;       // S MMAs of both tiles done with Q   (commit per issuer)
+  uint64_t q_full[2][2];  // [buffer][tile] TMA Q tile landed   (1 + tx)
+  uint64_t q_empty[2];    // [buffer] S MMAs done with the pair (commit per issuer)
   uint64_t kv_full[8];    // TMA K or V tile landed             (1 + tx)
   uint64_t kv_empty[8];   // both tiles' MMAs done with stage   (commit per issuer)
   uint64_t v_ready[8];    // V tile converted to fp16           (4 converter warps)
   uint64_t s_full[2];     // S_t = Q_t K^T complete             (commit)
-  uint64_t s_free[2];     // softmax has read S_t (split P only) (4 softmax warps)
-  uint64_t pv_done[2];    // P_t V MMA complete (split P only)  (commit)
   uint64_t p_full[2];     // P_t in TMEM, O_t rescaled          (4 softmax warps)
   uint64_t fin_full[2][2]; // [unit parity][tile] final m, l in shared (4 softmax warps)
   uint64_t o_full[2];     // last P_t V MMA of a unit done      (commit)
@@ -122,6 +123,8 @@ struct FwdShared {
   uint32_t conv_max[2][4];
   float m_fin[2][2][128];  // [unit parity][tile][row] final reference max (scaled log2)
   float l_fin[2][2][128];  // [unit parity][tile][row] final row sum
+  uint64_t s_free[2];     // softmax has read S_t (split P only) (4 softmax warps)
+  uint64_t pv_done[2];    // P_t V MMA complete (split P only)  (commit)
 };
 
 __device__ __forceinline__ void raise_abort(FwdShared &sb, int *err, int code) {
@@ -186,8 +189,8 @@ __global__ void __launch_bounds__(512, 1)
   __shared__ FwdShared sb;
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *sQ = smem;                        // 2 tiles
-  uint8_t *sKV = smem + 2 * C::kTileBytes;   // kStages tiles
+  uint8_t *sQ = smem;                                 // kQBufs pairs of tiles
+  uint8_t *sKV = smem + 2 * C::kQBufs * C::kTileBytes;  // kStages tiles
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -195,7 +198,9 @@ __global__ void __launch_bounds__(512, 1)
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&sb.q_full[t], 1);
+      mbar_init(&sb.q_full[0][t], 1);
+      mbar_init(&sb.q_full[1][t], 1);
+      mbar_init(&sb.q_empty[t], C::kSplitP ? 2 : 1);
       mbar_init(&sb.s_full[t], 1);
       mbar_init(&sb.s_free[t], 4);
       mbar_init(&sb.pv_done[t], 1);
@@ -206,7 +211,6 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.o_free[t], 4);
       mbar_init(&sb.mma_done[t], 1);
     }
-    mbar_init(&sb.q_empty, C::kSplitP ? 2 : 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sb.kv_full[s], 1);
       mbar_init(&sb.kv_empty[s], C::kSplitP ? 2 : 1);
@@ -331,10 +335,13 @@ __global__ void __launch_bounds__(512, 1)
             goto done;
           }
           tc_fence_after_sync();
+          ++steps;
+          tmem_st_32x32b_x32(tP + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st_32x32b_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        } else {
+          tmem_st_32x32b_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st_32x32b_x32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         }
-        ++steps;
-        tmem_st_32x32b_x32(tP + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st_32x32b_x32(tP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         // Exponent of the V tile this step multiplies (set by the converter;
         // waited here, after the P stores, to keep it off the exp path).
         const uint32_t vidx = kvb + 2 * j + 1;
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(512, 1)
         // commit is covered by this step's S_t commit, or waited above when
         // P is split from S): O_t holds its accumulated value.
         if (j > 0 && __any_sync(0xffffffffu, ofac != 1.0f)) {
-#pragma unroll
+#pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tO + c0, r);
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(512, 1)
             const bool valid = qrow < p.N;
             __nv_bfloat16 *orow = p.o + ((size_t)pend_bh * p.N + (valid ? qrow : 0)) * D;
             const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
-#pragma unroll
+#pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t r[32];
               tmem_ld_32x32b_x32(tO + c0, r);
@@ -582,7 +589,7 @@ __global__ void __launch_bounds__(512, 1)
         // Descriptor words: the low word carries the address / 16, stepped by
         // adds; the high word (stride 1024 B, 128-byte swizzle) is shared.
         const uint32_t dhi = sdesc_sw128_hi(1024);
-        const uint32_t a_lo = sdesc_sw128_lo(smem_addr(sQ), 16) + t * (C::kTileBytes >> 4);
+        const uint32_t a_lo0 = sdesc_sw128_lo(smem_addr(sQ), 16) + t * (C::kTileBytes >> 4);
         const uint32_t k_lo0 = sdesc_sw128_lo(smem_addr(sKV), 16);
         const uint32_t v_lo0 = sdesc_sw128_lo(smem_addr(sKV), C::kChunkBytes);
         const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
@@ -597,7 +604,8 @@ __global__ void __launch_bounds__(512, 1)
           unit_coords(p, kCausal, u, bh, mb);
           const int n1 = kv_tiles(p, kCausal, mb, 1);
           const int n_t = t ? n1 : kv_tiles(p, kCausal, mb, 0);
-  #pragma unroll 1
+          const int qb = uc % C::kQBufs;  // Q buffer of this unit
+#pragma unroll 1
           for (int j = 0; j <= n1; ++j) {
             const uint32_t kidx = kvb + 2 * j, vidx = kidx - 1;  // K_j and V_{j-1}
             const uint32_t ks = kidx % C::kStages, vs = vidx % C::kStages;
@@ -606,14 +614,15 @@ __global__ void __launch_bounds__(512, 1)
               // S_t = Q_t K_j^T once K_j has landed and the softmax has read
               // the previous S_t
               if (!mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag) ||
-                  (j == 0 && !mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) ||
+                  (j == 0 && !mbar_wait(&sb.q_full[qb][t], (uc / C::kQBufs) & 1, abort_flag)) ||
                   (s_cnt > 0 && !mbar_wait(&sb.s_free[t], (s_cnt - 1) & 1, abort_flag))) {
                 raise_abort(sb, p.err, kDevErrTimeout);
                 goto mma_exit_split;
               }
               ++s_cnt;
               tc_fence_after_sync();
-              issue_s<D>(tS, a_lo, k_lo0 + ks * (C::kTileBytes >> 4), dhi, idS);
+              issue_s<D>(tS, a_lo0 + qb * (2 * C::kTileBytes >> 4), k_lo0 + ks * (C::kTileBytes >> 4),
+                         dhi, idS);
               umma_commit(&sb.s_full[t]);
             }
             if (do_pv) {
@@ -633,7 +642,7 @@ __global__ void __launch_bounds__(512, 1)
             // with its Q tile); every stage gets one commit from each thread
             if (j < n1) umma_commit(&sb.kv_empty[ks]);
             if (j >= 1) umma_commit(&sb.kv_empty[vs]);
-            if (j == n1 - 1) umma_commit(&sb.q_empty);
+            if (j == n1 - 1) umma_commit(&sb.q_empty[qb]);
           }
           kvb += 2 * n1;
         }
@@ -696,7 +705,7 @@ __global__ void __launch_bounds__(512, 1)
               p_phase[t] ^= 1;
             }
             if (do_s && (j == 0 || !do_pv)) {
-              if ((j == 0 && !mbar_wait(&sb.q_full[t], uc & 1, abort_flag)) ||
+              if ((j == 0 && !mbar_wait(&sb.q_full[0][t], uc & 1, abort_flag)) ||
                   (!k_ready && !mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag))) {
                 raise_abort(sb, p.err, kDevErrTimeout);
                 goto mma_exit;
@@ -728,7 +737,7 @@ __global__ void __launch_bounds__(512, 1)
           }
           if (j < n1) umma_commit(&sb.kv_empty[ks]);   // both tiles are done with K_j
           if (j >= 1) umma_commit(&sb.kv_empty[vs]);   // ... and with V_{j-1}
-          if (j == n1 - 1) umma_commit(&sb.q_empty);   // and with both Q tiles
+          if (j == n1 - 1) umma_commit(&sb.q_empty[0]);  // and with both Q tiles
         }
         kvb += 2 * n1;
       }
@@ -752,14 +761,17 @@ __global__ void __launch_bounds__(512, 1)
         int bh, mb;
         unit_coords(p, kCausal, u, bh, mb);
         const int n1 = kv_tiles(p, kCausal, mb, 1);
-        if (uc > 0 && !mbar_wait(&sb.q_empty, (uc - 1) & 1, abort_flag)) {
+        // Q buffer qb was last used kQBufs units ago
+        const int qb = uc % C::kQBufs;
+        if (uc >= C::kQBufs && !mbar_wait(&sb.q_empty[qb], (uc / C::kQBufs - 1) & 1, abort_flag)) {
           raise_abort(sb, p.err, kDevErrTimeout);
           goto load_exit;
         }
         for (int t = 0; t < 2; ++t) {
-          mbar_arrive_expect_tx(&sb.q_full[t], C::kTileBytes);
+          mbar_arrive_expect_tx(&sb.q_full[qb][t], C::kTileBytes);
           for (int ch = 0; ch < C::kChunks; ++ch)
-            tma_load_3d_hint(sQ + t * C::kTileBytes + ch * C::kChunkBytes, &tm_q, &sb.q_full[t],
+            tma_load_3d_hint(sQ + (2 * qb + t) * C::kTileBytes + ch * C::kChunkBytes, &tm_q,
+                             &sb.q_full[qb][t],
                              ch * 64, mb * 256 + t * 128, bh, pol_q);
         }
         ++q_loads;
@@ -795,9 +807,11 @@ __global__ void __launch_bounds__(512, 1)
           if (p.test_drop_load && blockIdx.x == 0 && last == 0) continue;  // never issued
           mbar_wait(&sb.kv_full[s], (last / C::kStages) & 1, &never);
         }
-        if (q_loads > 0) {
-          mbar_wait(&sb.q_full[0], (q_loads - 1) & 1, &never);
-          mbar_wait(&sb.q_full[1], (q_loads - 1) & 1, &never);
+        // the last load of each Q buffer
+        for (uint32_t b = 0; b < (uint32_t)C::kQBufs && b < q_loads; ++b) {
+          const uint32_t last = q_loads - 1 - ((q_loads - 1 - b) % C::kQBufs);  // load index
+          mbar_wait(&sb.q_full[b][0], (last / C::kQBufs) & 1, &never);
+          mbar_wait(&sb.q_full[b][1], (last / C::kQBufs) & 1, &never);
         }
       }
     }

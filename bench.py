@@ -336,9 +336,16 @@ def main():
     extra = {}
     if args.all_workloads:
         for ow in WORKLOADS:
-            oms, _, _ = time_gpu(ow, max(5, args.steps // 5), 3, device)
+            # enough launches for about half a second, so the clock sampler
+            # sees the workload run
+            probe, _, _ = time_gpu(ow, 3, 3, device)
+            n = int(min(400, max(5, 500.0 / max(statistics.median(probe), 1e-3))))
+            with ClockSampler(device.index if world == 1 else local) as oclk:
+                oms, _, _ = time_gpu(ow, n, 3, device)
             m = statistics.median(oms)
-            extra[ow.name] = {"ms": round(m, 4), "tflops": round(ow.flops / m / 1e9, 1)}
+            c = oclk.summary()
+            extra[ow.name] = {"ms": round(m, 4), "tflops": round(ow.flops / m / 1e9, 1),
+                              "launches": n, "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
 
     if rank != 0:
         if world > 1:
