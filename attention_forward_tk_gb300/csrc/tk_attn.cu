@@ -9,7 +9,11 @@
 #include <cstring>
 #include <functional>
 #include <atomic>
+#include <memory>
 #include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "tk_attn.h"
 #include "tk_attn_fwd.cuh"
@@ -123,11 +127,66 @@ bool overlaps(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
   return a < b + nb && b < a + na;
 }
 
+// Causal unit lists (see SchedTable): every unit, in the unit order, goes to
+// the CTA with the fewest K/V steps so far (ties: lowest index), costing
+// n0 + n1 + 1 steps (both Q tiles' steps plus one for the unit's start-up).
+void build_sched(const FwdParams &p, int grid, SchedTable *tab) {
+  tab->n = 0;
+  if (p.num_units > kSchedCap || grid > kSchedMaxGrid) return;  // stride order
+  typedef std::pair<long long, int> Load;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int b = 0; b < grid; ++b) heap.push(Load(0, b));
+  std::vector<int> owner(p.num_units), count(grid, 0);
+  for (int u = 0; u < p.num_units; ++u) {
+    int bh, mb;
+    unit_coords(p, true, u, bh, mb);
+    const Load top = heap.top();
+    heap.pop();
+    owner[u] = top.second;
+    ++count[top.second];
+    heap.push(Load(top.first + kv_tiles(p, true, mb, 0) + kv_tiles(p, true, mb, 1) + 1,
+                   top.second));
+  }
+  tab->off[0] = 0;
+  for (int b = 0; b < grid; ++b) tab->off[b + 1] = (uint16_t)(tab->off[b] + count[b]);
+  std::vector<int> pos(tab->off, tab->off + grid);
+  for (int u = 0; u < p.num_units; ++u) tab->units[pos[owner[u]]++] = (uint16_t)u;
+  tab->n = p.num_units;
+}
+
+// Unit lists depend only on the shape; the last few are kept.
+struct SchedKey {
+  int BH, N, head_group, grid;
+  bool operator==(const SchedKey &o) const {
+    return BH == o.BH && N == o.N && head_group == o.head_group && grid == o.grid;
+  }
+};
+std::mutex g_sched_mu;
+std::vector<std::pair<SchedKey, std::shared_ptr<SchedTable>>> g_sched_cache;
+
+std::shared_ptr<SchedTable> sched_for(const FwdParams &p, int grid) {
+  const SchedKey key{p.BH, p.N, p.head_group, grid};
+  std::lock_guard<std::mutex> lock(g_sched_mu);
+  for (auto &e : g_sched_cache)
+    if (e.first == key) return e.second;
+  auto tab = std::make_shared<SchedTable>();
+  build_sched(p, grid, tab.get());
+  if (g_sched_cache.size() >= 8) g_sched_cache.erase(g_sched_cache.begin());
+  g_sched_cache.emplace_back(key, tab);
+  return tab;
+}
+
 template <int D, bool kCausal>
 cudaError_t launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                    const FwdParams &p, int grid, cudaStream_t stream) {
+  SchedFor<kCausal> tab;
+  std::shared_ptr<SchedTable> keep;
+  if constexpr (kCausal) {
+    keep = sched_for(p, grid);
+    tab = *keep;
+  }
   tk_attn_fwd_kernel<D, kCausal>
-      <<<grid, FwdCfg<D>::kThreads, FwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p);
+      <<<grid, FwdCfg<D>::kThreads, FwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p, tab);
   return cudaGetLastError();
 }
 

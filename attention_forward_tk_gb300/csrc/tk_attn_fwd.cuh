@@ -51,6 +51,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "sm103_ptx.cuh"
 
@@ -71,6 +72,23 @@ struct FwdParams {
   int test_drop_load;  // test hook: CTA 0 skips its first K load (0 = off)
   int head_group;      // causal unit order: heads per section (>= 1)
 };
+
+// Causal units differ in length (a query block visits only the keys up to
+// it), so causal launches carry each CTA's list of units, assigned on the
+// host greedily in the unit order: every unit goes to the CTA whose list is
+// shortest so far, counted in K/V steps.  That is the order a dynamic queue
+// would produce, with no claiming on the device.  Lists live in the kernel's
+// parameter space; more units than fit fall back to the stride order.
+constexpr int kSchedMaxGrid = 160;
+constexpr int kSchedCap = 12032;
+struct SchedTable {
+  int n;                               // units listed; 0 = stride order
+  uint16_t off[kSchedMaxGrid + 1];     // CTA b runs units[off[b] .. off[b+1])
+  uint16_t units[kSchedCap];
+};
+struct NoSchedTable {};
+template <bool kCausal>
+using SchedFor = typename std::conditional<kCausal, SchedTable, NoSchedTable>::type;
 
 template <int D>
 struct FwdCfg {
@@ -136,8 +154,8 @@ __device__ __forceinline__ void raise_abort(FwdShared &sb, int *err, int code) {
 // time share a head's K/V in L2.  Causal: heads are taken in sections of
 // head_group (sized on the host so a section's K/V fits in L2), and within a
 // section the longest query blocks come first.
-__device__ __forceinline__ void unit_coords(const FwdParams &p, bool causal, int u, int &bh,
-                                            int &mb) {
+__host__ __device__ __forceinline__ void unit_coords(const FwdParams &p, bool causal, int u,
+                                                     int &bh, int &mb) {
   if (causal) {
     const int per_section = p.head_group * p.num_mblocks;
     const int section = u / per_section;
@@ -152,11 +170,25 @@ __device__ __forceinline__ void unit_coords(const FwdParams &p, bool causal, int
 }
 
 // Number of 128-key tiles Q tile t of block mb visits.
-__device__ __forceinline__ int kv_tiles(const FwdParams &p, bool causal, int mb, int t) {
+__host__ __device__ __forceinline__ int kv_tiles(const FwdParams &p, bool causal, int mb, int t) {
   const int nkv = (p.N + 127) / 128;
   if (!causal) return nkv;
   const int last_row = min(mb * 256 + t * 128 + 127, p.N - 1);
   return last_row / 128 + 1;
+}
+
+// The uc-th work unit of this CTA, or -1 when none is left.
+template <bool kCausal>
+__device__ __forceinline__ int unit_at(const SchedFor<kCausal> &tab, const FwdParams &p,
+                                       int uc) {
+  if constexpr (kCausal) {
+    if (tab.n > 0) {
+      const int i = tab.off[blockIdx.x] + uc;
+      return i < tab.off[blockIdx.x + 1] ? (int)tab.units[i] : -1;
+    }
+  }
+  const int u = blockIdx.x + uc * (int)gridDim.x;
+  return u < p.num_units ? u : -1;
 }
 
 // S = Q K^T for one Q tile: 16 head-dim columns (32 B of a swizzled row) per MMA.
@@ -183,7 +215,8 @@ template <int D, bool kCausal>
 __global__ void __launch_bounds__(512, 1)
     tk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p,
+                       const __grid_constant__ SchedFor<kCausal> tab) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdShared sb;
@@ -247,8 +280,9 @@ __global__ void __launch_bounds__(512, 1)
     uint32_t s_phase = 0;
     uint32_t steps = 0;  // S tiles this warp has processed (all units): P V MMAs issued before
     uint32_t kvb = 0;  // K/V load index of this unit's K_0
-    int uc = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+    for (int uc = 0;; ++uc) {
+      const int u = unit_at<kCausal>(tab, p, uc);
+      if (u < 0) break;
       int bh, mb;
       unit_coords(p, kCausal, u, bh, mb);
       const int n_t = kv_tiles(p, kCausal, mb, t);
@@ -418,9 +452,9 @@ __global__ void __launch_bounds__(512, 1)
     uint32_t conv_count = 0;  // V tiles converted (conv_bar phases)
     // the unit whose epilogue is pending
     int pend_bh = -1, pend_mb = 0, pend_uc = 0, pend_e[2] = {0, 0};
-    int uc = 0;
-    for (int u = blockIdx.x;; u += gridDim.x, ++uc) {
-      const bool have_unit = u < p.num_units;
+    for (int uc = 0;; ++uc) {
+      const int u = unit_at<kCausal>(tab, p, uc);
+      const bool have_unit = u >= 0;
       int bh = 0, mb = 0, n0 = 0, n1 = 0;
       if (have_unit) {
         unit_coords(p, kCausal, u, bh, mb);
@@ -598,8 +632,9 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t p_phase = 0;
         uint32_t s_cnt = 0;  // S MMAs issued (split P: s_free phases)
         uint32_t kvb = 0;
-        int uc = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+        for (int uc = 0;; ++uc) {
+          const int u = unit_at<kCausal>(tab, p, uc);
+          if (u < 0) break;
           int bh, mb;
           unit_coords(p, kCausal, u, bh, mb);
           const int n1 = kv_tiles(p, kCausal, mb, 1);
@@ -673,8 +708,9 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t v_lo0 = sdesc_sw128_lo(smem_addr(sKV), C::kChunkBytes);
       uint32_t p_phase[2] = {0, 0};
       uint32_t kvb = 0;
-      int uc = 0;
-      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+      for (int uc = 0;; ++uc) {
+        const int u = unit_at<kCausal>(tab, p, uc);
+        if (u < 0) break;
         int bh, mb;
         unit_coords(p, kCausal, u, bh, mb);
         const int n0 = kv_tiles(p, kCausal, mb, 0);
@@ -754,10 +790,11 @@ __global__ void __launch_bounds__(512, 1)
       // ---------------------------------------------------------- TMA producer
       uint32_t kv_idx = 0;
       uint32_t q_loads = 0;  // Q tile pairs issued
-      int uc = 0;
       const uint64_t pol_kv = l2_policy_evict_last();
       const uint64_t pol_q = l2_policy_evict_first();
-      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++uc) {
+      for (int uc = 0;; ++uc) {
+        const int u = unit_at<kCausal>(tab, p, uc);
+        if (u < 0) break;
         int bh, mb;
         unit_coords(p, kCausal, u, bh, mb);
         const int n1 = kv_tiles(p, kCausal, mb, 1);

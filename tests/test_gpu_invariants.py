@@ -154,3 +154,31 @@ def test_device_timeout_is_reported_and_recoverable(tk_lib, oracle_lib):
     o_ref, lse_ref = oracle_lib.attention(q, k, v, 0.125, False)
     assert np.abs(o.float().cpu().double().numpy() - o_ref).max() <= TOL_O_MAX
     assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= TOL_LSE_MAX
+
+
+def test_causal_unit_lists_mixed_lengths(tk_lib, oracle_lib):
+    # 2 * 20 heads * 5 query blocks = 200 causal units of five lengths on 152
+    # CTAs: the host-built unit lists give CTAs different unit counts.
+    shape = (2, 20, 1280, 128)
+    q, k, v = draw(shape, seed=208)
+    scale = 1 / math.sqrt(128)
+    o, lse = run_gpu(tk_lib, q, k, v, scale, True)
+    o_ref, lse_ref = oracle_lib.attention(q, k, v, scale, True)
+    assert np.abs(o - o_ref).max() <= TOL_O_MAX
+    assert np.abs(o - o_ref).mean() <= TOL_O_MEAN
+    assert np.abs(lse - lse_ref).max() <= TOL_LSE_MAX
+
+
+def test_causal_more_units_than_the_list_holds(tk_lib, oracle_lib):
+    # 1 * 12100 heads * 1 query block: more causal units than a launch's unit
+    # lists hold, so the kernel takes them in stride order.  Checked on a few
+    # heads spread over the range (N = 16: one ragged tile per head).
+    B, H, N, D = 1, 12100, 16, 64
+    q, k, v = draw((B, H, N, D), seed=209)
+    scale = 0.125
+    o, lse = run_gpu(tk_lib, q, k, v, scale, True)
+    heads = [0, 1, 151, 152, 6049, 12098, 12099]
+    sub = (q[:, heads], k[:, heads], v[:, heads])
+    o_ref, lse_ref = oracle_lib.attention(*sub, scale, True)
+    assert np.abs(o[:, heads] - o_ref).max() <= TOL_O_MAX
+    assert np.abs(lse[:, heads] - lse_ref).max() <= TOL_LSE_MAX
