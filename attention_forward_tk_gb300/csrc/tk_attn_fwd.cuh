@@ -143,6 +143,7 @@ struct FwdShared {
   float l_fin[2][2][128];  // [unit parity][tile][row] final row sum
   uint64_t s_free[2];     // softmax has read S_t (split P only) (4 softmax warps)
   uint64_t pv_done[2];    // P_t V MMA complete (split P only)  (commit)
+  uint64_t exp_turn[2];   // split P: tile t may run its exponentials (4 warps of the other tile)
 };
 
 __device__ __forceinline__ void raise_abort(FwdShared &sb, int *err, int code) {
@@ -237,6 +238,7 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.s_full[t], 1);
       mbar_init(&sb.s_free[t], 4);
       mbar_init(&sb.pv_done[t], 1);
+      mbar_init(&sb.exp_turn[t], 4);
       mbar_init(&sb.p_full[t], 4);
       mbar_init(&sb.fin_full[0][t], 4);
       mbar_init(&sb.fin_full[1][t], 4);
@@ -250,6 +252,8 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&sb.v_ready[s], 4);
     }
     mbar_init(&sb.conv_bar, 4);
+    // tile 0 takes the first exponential turn
+    for (int i = 0; i < 4; ++i) mbar_arrive(&sb.exp_turn[0]);
     sb.abort = 0;
     fence_mbar_init();
   }
@@ -279,6 +283,7 @@ __global__ void __launch_bounds__(512, 1)
     const float c = p.scale_log2;
     uint32_t s_phase = 0;
     uint32_t steps = 0;  // S tiles this warp has processed (all units): P V MMAs issued before
+    uint32_t turns = 0;  // split P: exponential turns this tile has taken
     uint32_t kvb = 0;  // K/V load index of this unit's K_0
     for (int uc = 0;; ++uc) {
       const int u = unit_at<kCausal>(tab, p, uc);
@@ -286,6 +291,7 @@ __global__ void __launch_bounds__(512, 1)
       int bh, mb;
       unit_coords(p, kCausal, u, bh, mb);
       const int n_t = kv_tiles(p, kCausal, mb, t);
+      const int n0 = kv_tiles(p, kCausal, mb, 0);
       const int n1 = kv_tiles(p, kCausal, mb, 1);
       const int qrow = mb * 256 + t * 128 + row;  // global query index
       float m_run = -INFINITY, l_run = 0.f;
@@ -344,6 +350,16 @@ __global__ void __launch_bounds__(512, 1)
         const uint64_t c2 = f2_pack(c, c);
         const uint64_t nm2 = f2_pack(-m_run, -m_run);
         uint64_t la = 0, lb = 0;  // (+0.f, +0.f) pairs
+        // Split P: the two tiles' softmax warps of an SM sub-partition take
+        // turns at the exponentials (the special-function unit is the shared
+        // bottleneck), so each one's other work overlaps the other's
+        // exponentials.  Turns pair step j of tile 0 with step j of tile 1;
+        // a causal unit's last tile-1 step has no partner and takes no turn.
+        const bool take_turn = C::kSplitP && (t == 0 || j < n0);
+        if (take_turn && !mbar_wait(&sb.exp_turn[t], turns & 1, abort_flag)) {
+          raise_abort(sb, p.err, kDevErrTimeout);
+          goto done;
+        }
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
@@ -360,6 +376,11 @@ __global__ void __launch_bounds__(512, 1)
           pk[i + 1] = pack_f16x2(p2, p3);
           la = f2_add(la, f2_pack(p0, p1));
           lb = f2_add(lb, f2_pack(p2, p3));
+        }
+        if (take_turn) {
+          ++turns;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sb.exp_turn[t ^ 1]);
         }
         if constexpr (C::kSplitP) {
           // The previous P_t V MMA must be done reading P_t (and writing O_t,
