@@ -9,6 +9,9 @@ precision, so the GPU kernels have something independent to be checked against.
 Contents
   attention_rows   plain definition (C, OpenMP, fp64) for chosen rows
   attention        the same for every row of a [B, H, N, D] problem
+  attention_qk_rows, attention_qk
+                   the same definition for Nq queries against Nk keys
+                   (inference shape); causal aligned to the last key
   tiled_online_softmax
                    numpy restatement of the tile-by-tile online-softmax
                    recurrence the kernel examples on the pages use, both in
@@ -22,11 +25,14 @@ write-up (88811315.cn, post 77732); the causal mask and the log-sum-exp follow
 the plainest reading of the requested interface (keys j <= i visible; natural
 log over scaled, masked scores).
 """
-from .brute import attention, attention_rows, build, lib_path, max_threads
+from .brute import (attention, attention_qk, attention_qk_rows, attention_rows, build, lib_path,
+                    max_threads)
 from .tiled import tiled_online_softmax
 
 __all__ = [
     "attention",
+    "attention_qk",
+    "attention_qk_rows",
     "attention_rows",
     "build",
     "lib_path",

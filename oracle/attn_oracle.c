@@ -149,6 +149,93 @@ int attn_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   return failed ? -1 : used;
 }
 
+/*
+ * Queries and keys of different lengths (Nq query rows, Nk keys per slice),
+ * the shape of attention at inference time: a block of new queries against
+ * a longer run of cached keys.  Same definition as above, with the visible
+ * keys of query i being all j < Nk, or, under the causal mask aligned to
+ * the end of the key sequence, j <= i + (Nk - Nq) (query i is the
+ * (Nk - Nq + i)-th position of the sequence).  For Nq == Nk this is the mask
+ * above.  Neither page fixes the alignment for Nq != Nk; this is the reading
+ * where the queries are the last Nq positions of the sequence.
+ *
+ *   q  bf16 bits [BH, Nq, D];  k, v  bf16 bits [BH, Nk, D]
+ *   rows      flat query-row indices bh*Nq + i (NULL = every row, in order)
+ *   o, lse    out: [nrows, D] and [nrows] doubles
+ * Returns the number of threads used, or -1 on a bad argument (including a
+ * causal Nq > Nk, where the first queries would see no key).
+ */
+static void one_row_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       int64_t Nq, int64_t Nk, int64_t D, double scale, int causal,
+                       int64_t bh, int64_t i, double *scores, double *o_row, double *lse_out) {
+  const uint16_t *qi = q + (bh * Nq + i) * D;
+  const uint16_t *kb = k + bh * Nk * D;
+  const uint16_t *vb = v + bh * Nk * D;
+  const int64_t nvis = causal ? (i + (Nk - Nq) + 1) : Nk;
+  double m = -INFINITY;
+  for (int64_t j = 0; j < nvis; ++j) {
+    const uint16_t *kj = kb + j * D;
+    double dot = 0.0;
+    for (int64_t d = 0; d < D; ++d) dot += widen_bf16(qi[d]) * widen_bf16(kj[d]);
+    double s = scale * dot;
+    scores[j] = s;
+    if (s > m) m = s;
+  }
+  double z = 0.0;
+  for (int64_t j = 0; j < nvis; ++j) z += exp(scores[j] - m);
+  double lse = m + log(z);
+  for (int64_t d = 0; d < D; ++d) o_row[d] = 0.0;
+  for (int64_t j = 0; j < nvis; ++j) {
+    double p = exp(scores[j] - lse);
+    const uint16_t *vj = vb + j * D;
+    for (int64_t d = 0; d < D; ++d) o_row[d] += p * widen_bf16(vj[d]);
+  }
+  *lse_out = lse;
+}
+
+int attn_oracle_rows_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t BH,
+                        int64_t Nq, int64_t Nk, int64_t D, double scale, int causal,
+                        const int64_t *rows, int64_t nrows, double *o, double *lse,
+                        int nthreads) {
+  if (!q || !k || !v || !o || !lse || BH <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return -1;
+  if (causal && Nq > Nk) return -1;
+  int64_t total = rows ? nrows : BH * Nq;
+  if (total < 0) return -1;
+  if (rows) {
+    for (int64_t r = 0; r < nrows; ++r)
+      if (rows[r] < 0 || rows[r] >= BH * Nq) return -1;
+  }
+  int used = 1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+  {
+#pragma omp single
+    used = omp_get_num_threads();
+  }
+#else
+  (void)nthreads;
+#endif
+  int failed = 0;
+#pragma omp parallel
+  {
+    double *scores = (double *)malloc((size_t)Nk * sizeof(double));
+    if (!scores) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t r = 0; r < total; ++r) {
+      if (!scores) continue;
+      int64_t flat = rows ? rows[r] : r;
+      one_row_qk(q, k, v, Nq, Nk, D, scale, causal, flat / Nq, flat % Nq, scores, o + r * D,
+                 lse + r);
+    }
+    free(scores);
+  }
+  return failed ? -1 : used;
+}
+
 /* Threads an OpenMP region would use by default (for reporting). */
 int attn_oracle_max_threads(void) {
 #ifdef _OPENMP

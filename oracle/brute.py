@@ -59,6 +59,14 @@ def _load():
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
             ]
+            lib.attn_oracle_rows_qk.restype = ctypes.c_int
+            lib.attn_oracle_rows_qk.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_double, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ]
             lib.attn_oracle_max_threads.restype = ctypes.c_int
             lib.attn_oracle_max_threads.argtypes = []
             _lib = lib
@@ -127,4 +135,46 @@ def attention(q, k, v, scale: float, causal: bool, nthreads: int = 0):
     """Every row: returns (o [..., N, D] float64, lse [..., N] float64)."""
     qb = _bf16_bits(q)
     o, lse, _ = attention_rows(qb, k, v, scale, causal, None, None, nthreads)
+    return o.reshape(qb.shape), lse.reshape(qb.shape[:-1])
+
+
+def attention_qk_rows(q, k, v, scale: float, causal: bool, rows=None, nthreads: int = 0):
+    """O and LSE (float64) for queries and keys of different lengths.
+
+    q : bf16 bits [..., Nq, D];  k, v : bf16 bits [..., Nk, D] (same leading dims)
+    causal: key j visible to query i iff j <= i + (Nk - Nq) (the queries are
+    the last Nq positions of the sequence); requires Nq <= Nk.
+    rows : flat query-row indices bh*Nq + i (None = all rows, in order)
+    Returns (o [nrows, D], lse [nrows], threads_used).
+    """
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    if kb.shape != vb.shape or qb.ndim < 2 or qb.shape[:-2] != kb.shape[:-2] or \
+            qb.shape[-1] != kb.shape[-1]:
+        raise ValueError("q [..., Nq, D] and k, v [..., Nk, D] must share leading dims and D")
+    Nq, Nk, D = int(qb.shape[-2]), int(kb.shape[-2]), int(qb.shape[-1])
+    BH = int(qb.size // (Nq * D)) if Nq * D > 0 else 0
+    if rows is None:
+        nrows = BH * Nq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = int(rows_arr.size)
+    o = np.empty((nrows, D), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    if nrows == 0:
+        return o, lse, 0
+    used = _load().attn_oracle_rows_qk(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, BH, Nq, Nk, D,
+        float(scale), int(bool(causal)),
+        rows_arr.ctypes.data if rows_arr is not None else None, nrows,
+        o.ctypes.data, lse.ctypes.data, int(nthreads))
+    if used < 0:
+        raise ValueError("attn_oracle_rows_qk rejected its arguments")
+    return o, lse, int(used)
+
+
+def attention_qk(q, k, v, scale: float, causal: bool, nthreads: int = 0):
+    """Every query row: returns (o [..., Nq, D] float64, lse [..., Nq] float64)."""
+    qb = _bf16_bits(q)
+    o, lse, _ = attention_qk_rows(qb, k, v, scale, causal, None, nthreads)
     return o.reshape(qb.shape), lse.reshape(qb.shape[:-1])

@@ -228,3 +228,97 @@ def test_rejects_bad_rows(oracle_lib):
     q, k, v = draw((1, 1, 4, 8), seed=24)
     with pytest.raises(ValueError):
         oracle_lib.attention_rows(q, k, v, 0.25, False, [4])
+
+
+# --------------------------------------------------------------------------
+# queries and keys of different lengths (inference shape)
+
+
+def qk_inputs(seed, BH=2, Nq=5, Nk=23, D=64):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((1, BH, Nq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((1, BH, Nk, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((1, BH, Nk, D), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_qk_zero_query_is_uniform(oracle_lib, causal):
+    # Q = 0: every visible score is 0, so O is the mean of the visible V rows
+    # and LSE = ln(#visible): all Nk keys, or Nk - Nq + 1 + i under the mask
+    # aligned to the last key.
+    _, k, v = qk_inputs(301)
+    q = torch.zeros((1, 2, 5, 64), dtype=torch.bfloat16)
+    o, lse = oracle_lib.attention_qk(q, k, v, 0.3, causal)
+    vd = widen(v)[0]
+    Nq, Nk = 5, 23
+    for i in range(Nq):
+        n = (Nk - Nq + 1 + i) if causal else Nk
+        np.testing.assert_allclose(o[0, :, i], vd[:, :n].mean(axis=1), atol=1e-12)
+        np.testing.assert_allclose(lse[0, :, i], math.log(n), atol=1e-12)
+
+
+def test_qk_single_key(oracle_lib):
+    q, k, v = qk_inputs(302, Nk=1)
+    q = q[:, :, :1]
+    o, lse = oracle_lib.attention_qk(q, k, v, 0.125, False)
+    np.testing.assert_allclose(o, widen(v), atol=1e-12)
+    ref = 0.125 * (widen(q)[0, :, 0] * widen(k)[0, :, 0]).sum(-1)
+    np.testing.assert_allclose(lse[0, :, 0], ref, atol=1e-12)
+
+
+def test_qk_causal_last_query_sees_every_key(oracle_lib):
+    # under the mask aligned to the last key, the last query sees all Nk keys:
+    # it must equal the unmasked result for that row
+    q, k, v = qk_inputs(303)
+    oc, lc = oracle_lib.attention_qk(q, k, v, 0.1, True)
+    on, ln_ = oracle_lib.attention_qk(q, k, v, 0.1, False)
+    np.testing.assert_allclose(oc[0, :, -1], on[0, :, -1], atol=1e-12)
+    np.testing.assert_allclose(lc[0, :, -1], ln_[0, :, -1], atol=1e-12)
+    # and the first query sees Nk - Nq + 1 keys: its LSE is below the full one
+    assert np.all(lc[0, :, 0] < ln_[0, :, 0])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_qk_matches_torch_sdpa_float64(oracle_lib, causal):
+    # special case that reduces to a library routine: float64 scaled-dot-
+    # product attention with an explicit mask (key j <= i + Nk - Nq)
+    q, k, v = qk_inputs(304, BH=3, Nq=7, Nk=40)
+    Nq, Nk = 7, 40
+    qd, kd, vd = (t.double() for t in (q, k, v))
+    scale = 0.11
+    mask = None
+    if causal:
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        mask = j <= i + (Nk - Nq)
+    ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, attn_mask=mask, scale=scale)
+    s = scale * qd @ kd.transpose(-1, -2)
+    if causal:
+        s = s.masked_fill(~mask, float("-inf"))
+    ref_lse = torch.logsumexp(s, dim=-1)
+    o, lse = oracle_lib.attention_qk(q, k, v, scale, causal)
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), atol=1e-12)
+
+
+def test_qk_key_splits_combine_by_lse(oracle_lib):
+    # the identity a split over keys relies on: with O_s, LSE_s the results on
+    # disjoint key ranges, LSE = ln sum_s exp(LSE_s) and O = sum_s
+    # exp(LSE_s - LSE) O_s reproduce the result over all keys
+    q, k, v = qk_inputs(305, Nk=40)
+    o, lse = oracle_lib.attention_qk(q, k, v, 0.125, False)
+    bounds = [0, 13, 14, 40]
+    parts = [oracle_lib.attention_qk(q, k[:, :, a:b], v[:, :, a:b], 0.125, False)
+             for a, b in zip(bounds[:-1], bounds[1:])]
+    lses = np.stack([pl for _, pl in parts])
+    tot = np.log(np.exp(lses - lses.max(0)).sum(0)) + lses.max(0)
+    comb = sum(np.exp(pl - tot)[..., None] * po for po, pl in parts)
+    np.testing.assert_allclose(tot, lse, atol=1e-12)
+    np.testing.assert_allclose(comb, o, atol=1e-12)
+
+
+def test_qk_rejects_causal_with_more_queries_than_keys(oracle_lib):
+    q, k, v = qk_inputs(306, Nq=5, Nk=3)
+    with pytest.raises(ValueError):
+        oracle_lib.attention_qk(q, k, v, 0.1, True)
