@@ -10,12 +10,15 @@ from .api import (  # noqa: F401
     TkAttnError,
     attention_forward,
     attention_forward_host,
+    attention_forward_splitkv,
     last_device_error,
     library,
     status_string,
     tk_attn_check_args,
     tk_attn_fwd,
+    tk_attn_fwd_splitkv,
     tk_attn_last_device_error,
+    tk_attn_splitkv_workspace_bytes,
     tk_attn_status_string,
     tk_attn_version,
     version,

@@ -30,6 +30,8 @@ TK_ATTN_ERR_DEVICE_TIMEOUT = -5
 # every symbol include/tk_attn.h declares
 EXPORTED = (
     "tk_attn_fwd",
+    "tk_attn_fwd_splitkv",
+    "tk_attn_splitkv_workspace_bytes",
     "tk_attn_check_args",
     "tk_attn_status_string",
     "tk_attn_version",
@@ -67,6 +69,11 @@ def library() -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.tk_attn_fwd.restype = i
         lib.tk_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.tk_attn_fwd_splitkv.restype = i
+        lib.tk_attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
+                                            ctypes.c_size_t, vp]
+        lib.tk_attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.tk_attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.tk_attn_check_args.restype = i
         lib.tk_attn_check_args.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i]
         lib.tk_attn_status_string.restype = ctypes.c_char_p
@@ -88,6 +95,19 @@ def tk_attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int
                 D: int, scale: float, causal: int, stream: int) -> int:
     return int(library().tk_attn_fwd(q, k, v, o, lse, B, H, N, D, ctypes.c_float(scale),
                                      int(causal), stream))
+
+
+def tk_attn_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Nq: int,
+                        Nk: int, D: int, scale: float, num_splits: int, workspace: int,
+                        workspace_bytes: int, stream: int) -> int:
+    return int(library().tk_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, D,
+                                             ctypes.c_float(scale), int(num_splits), workspace,
+                                             int(workspace_bytes), stream))
+
+
+def tk_attn_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, D: int,
+                                    num_splits: int) -> int:
+    return int(library().tk_attn_splitkv_workspace_bytes(B, H, Nq, Nk, D, int(num_splits)))
 
 
 def tk_attn_check_args(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int,
@@ -162,6 +182,39 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     _check(tk_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                        lse.data_ptr(), B, H, N, D, float(scale), int(bool(causal)),
                        _stream_handle(stream)))
+    return out, lse
+
+
+def attention_forward_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0,
+                              out=None, lse=None, workspace=None, stream=None):
+    """O, LSE for bf16 CUDA tensors q [B, H, Nq, D] against k, v [B, H, Nk, D],
+    unmasked, with the keys split into `num_splits` ranges (0: the library's
+    default).  The workspace is allocated by torch when not given.  Enqueued
+    on `stream`; returns immediately.
+    """
+    import torch
+    if q.dim() != 4 or k.shape != v.shape or k.dim() != 4 or q.shape[:2] != k.shape[:2] or \
+            q.shape[3] != k.shape[3]:
+        raise ValueError("q must be [B, H, Nq, D] and k, v [B, H, Nk, D]")
+    B, H, Nq, D = (int(x) for x in q.shape)
+    Nk = int(k.shape[2])
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    need = tk_attn_splitkv_workspace_bytes(B, H, Nq, Nk, D, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(tk_attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), B, H, Nq, Nk, D, float(scale), int(num_splits),
+                               ws_ptr, ws_bytes, _stream_handle(stream)))
     return out, lse
 
 

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "tk_attn.h"
+#include "tk_attn_combine.cuh"
 #include "tk_attn_fwd.cuh"
 
 namespace tkattn {
@@ -43,9 +44,9 @@ std::atomic<int> g_test_drop_load{0};
 std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 
-template <int D, bool kCausal>
+template <int D, bool kCausal, bool kSplit = false>
 int configure_kernel() {
-  auto kern = tk_attn_fwd_kernel<D, kCausal>;
+  auto kern = tk_attn_fwd_kernel<D, kCausal, kSplit>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            FwdCfg<D>::kSmemAlloc) != cudaSuccess)
     return TK_ATTN_ERR_LAUNCH;
@@ -74,6 +75,8 @@ void init_device(int dev, DeviceState &ds) {
   if (!st) st = configure_kernel<64, true>();
   if (!st) st = configure_kernel<128, false>();
   if (!st) st = configure_kernel<128, true>();
+  if (!st) st = configure_kernel<64, false, true>();
+  if (!st) st = configure_kernel<128, false, true>();
   if (!st && cudaGetSymbolAddress(reinterpret_cast<void **>(&ds.err_word), g_dev_error) !=
                  cudaSuccess)
     st = TK_ATTN_ERR_LAUNCH;
@@ -176,7 +179,7 @@ std::shared_ptr<SchedTable> sched_for(const FwdParams &p, int grid) {
   return tab;
 }
 
-template <int D, bool kCausal>
+template <int D, bool kCausal, bool kSplit = false>
 cudaError_t launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                    const FwdParams &p, int grid, cudaStream_t stream) {
   SchedFor<kCausal> tab;
@@ -185,7 +188,7 @@ cudaError_t launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorM
     keep = sched_for(p, grid);
     tab = *keep;
   }
-  tk_attn_fwd_kernel<D, kCausal>
+  tk_attn_fwd_kernel<D, kCausal, kSplit>
       <<<grid, FwdCfg<D>::kThreads, FwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p, tab);
   return cudaGetLastError();
 }
@@ -241,6 +244,11 @@ extern "C" int tk_attn_fwd(const void *q, const void *k, const void *v, void *o,
   p.err = ds->err_word;
   p.BH = BH;
   p.N = N;
+  p.Nk = N;
+  p.num_splits = 1;
+  p.split_tiles = (N + 127) / 128;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
   p.num_mblocks = (N + 255) / 256;
   p.num_units = BH * p.num_mblocks;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
@@ -263,6 +271,159 @@ extern "C" int tk_attn_fwd(const void *q, const void *k, const void *v, void *o,
   else
     e = causal ? launch<128, true>(tq, tk, tv, p, grid, s)
                : launch<128, false>(tq, tk, tv, p, grid, s);
+  return e == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------- split over keys
+
+namespace tkattn {
+namespace {
+
+// Ranges for a split over keys: `requested` (> 0), or by default the count
+// that minimises the launch's makespan in K/V steps, rounds x (T + c), when
+// that beats one range by at least 10%: units
+// = (slice, query block) pairs x ranges run in ceil(units / SMs) rounds of
+// one unit per SM, and a unit of T tiles costs about c = 3 tiles more for
+// its start and end.  At most one range per 128-key tile, and no empty
+// range: ranges of T tiles, S = ceil(nkv / T).
+void resolve_splits(int requested, long long units_q, int nkv, int num_sms, int *S, int *T) {
+  auto fit = [nkv](long long s, int *S_, int *T_) {
+    if (s > nkv) s = nkv;
+    if (s < 1) s = 1;
+    *T_ = (int)((nkv + s - 1) / s);
+    *S_ = (nkv + *T_ - 1) / *T_;
+  };
+  if (requested > 0) {
+    fit(requested, S, T);
+    return;
+  }
+  constexpr long long kUnitCost = 3;
+  long long best = -1, one = -1;
+  for (long long s = 1; s <= nkv && s <= 8LL * num_sms; ++s) {
+    int s2, t2;
+    fit(s, &s2, &t2);
+    if (s2 != s) continue;  // the same ranges as a smaller count
+    const long long rounds = (units_q * s2 + num_sms - 1) / num_sms;
+    const long long cost = rounds * (t2 + kUnitCost);
+    if (s2 == 1) one = cost;
+    if (best < 0 || cost < best) {
+      best = cost;
+      *S = s2;
+      *T = t2;
+    }
+  }
+  // The ranges' fp32 partial results make a round trip through memory and a
+  // second kernel: split only for a clearly shorter makespan (>= 10%).
+  if (best < 0 || 10 * best > 9 * one) fit(1, S, T);
+}
+
+size_t split_workspace(long long BH, int Nq, int D, int S) {
+  return S > 1 ? (size_t)S * (size_t)BH * (size_t)Nq * (size_t)(D + 1) * sizeof(float) : 0;
+}
+
+int check_splitkv_args(const void *q, const void *k, const void *v, const void *o,
+                       const float *lse, int B, int H, int Nq, int Nk, int D, float scale) {
+  if (!q || !k || !v || !o || !lse) return TK_ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return TK_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TK_ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return TK_ATTN_ERR_UNSUPPORTED;
+  const uintptr_t pq = (uintptr_t)q, pk = (uintptr_t)k, pv = (uintptr_t)v, po = (uintptr_t)o,
+                  pl = (uintptr_t)lse;
+  if ((pq | pk | pv | po | pl) & 15u) return TK_ATTN_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  const long long nkv = (Nk + 127LL) / 128;
+  // units (slice x query block x range) and their claims must fit an int
+  if (BH > 0x7fffffffLL || BH * ((Nq + 255LL) / 256) * nkv > 0x7fffffffLL)
+    return TK_ATTN_ERR_UNSUPPORTED;
+  const unsigned long long qbytes = (unsigned long long)BH * Nq * D * 2ull;
+  const unsigned long long kbytes = (unsigned long long)BH * Nk * D * 2ull;
+  if (qbytes >= (1ull << 40) || kbytes >= (1ull << 40)) return TK_ATTN_ERR_UNSUPPORTED;
+  const size_t lbytes = (size_t)BH * (size_t)Nq * 4u;
+  if (overlaps(po, qbytes, pl, lbytes) || overlaps(po, qbytes, pq, qbytes) ||
+      overlaps(po, qbytes, pk, kbytes) || overlaps(po, qbytes, pv, kbytes) ||
+      overlaps(pl, lbytes, pq, qbytes) || overlaps(pl, lbytes, pk, kbytes) ||
+      overlaps(pl, lbytes, pv, kbytes))
+    return TK_ATTN_ERR_INVALID_ARG;
+  return TK_ATTN_OK;
+}
+
+}  // namespace
+}  // namespace tkattn
+
+extern "C" size_t tk_attn_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int D,
+                                                  int num_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (D != 64 && D != 128)) return 0;
+  int st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return 0;
+  const long long BH = (long long)B * H;
+  int S, T;
+  resolve_splits(num_splits, BH * ((Nq + 255LL) / 256), (Nk + 127) / 128, ds->num_sms, &S, &T);
+  return split_workspace(BH, Nq, D, S);
+}
+
+extern "C" int tk_attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int B, int H, int Nq, int Nk, int D, float scale,
+                                   int num_splits, void *workspace, size_t workspace_bytes,
+                                   tk_attn_stream_t stream) {
+  int st = check_splitkv_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale);
+  if (st) return st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  const int BH = B * H;
+  const int nmb = (Nq + 255) / 256, nkv = (Nk + 127) / 128;
+  int S, T;
+  resolve_splits(num_splits, (long long)BH * nmb, nkv, ds->num_sms, &S, &T);
+  const size_t need = split_workspace(BH, Nq, D, S);
+  if (S > 1) {
+    const uintptr_t pw = (uintptr_t)workspace;
+    if (!workspace || (pw & 15u) || workspace_bytes < need) return TK_ATTN_ERR_INVALID_ARG;
+    const size_t qbytes = (size_t)BH * Nq * D * 2, kbytes = (size_t)BH * Nk * D * 2;
+    if (overlaps(pw, need, (uintptr_t)q, qbytes) || overlaps(pw, need, (uintptr_t)k, kbytes) ||
+        overlaps(pw, need, (uintptr_t)v, kbytes) || overlaps(pw, need, (uintptr_t)o, qbytes) ||
+        overlaps(pw, need, (uintptr_t)lse, (size_t)BH * Nq * 4))
+      return TK_ATTN_ERR_INVALID_ARG;
+  }
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, BH, Nq, D) || !make_map(&tk, k, BH, Nk, D) ||
+      !make_map(&tv, v, BH, Nk, D))
+    return TK_ATTN_ERR_LAUNCH;
+  FwdParams p;
+  p.o = static_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.err = ds->err_word;
+  p.BH = BH;
+  p.N = Nq;
+  p.Nk = Nk;
+  p.num_mblocks = nmb;
+  p.num_splits = S;
+  p.split_tiles = T;
+  p.o_part = S > 1 ? static_cast<float *>(workspace) : nullptr;
+  p.lse_part = S > 1 ? static_cast<float *>(workspace) + (size_t)S * BH * Nq * D : nullptr;
+  p.num_units = BH * nmb * S;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.test_drop_load = g_test_drop_load.load(std::memory_order_relaxed);
+  p.head_group = 1;
+  const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (S == 1) {  // one range: the single-pass kernel writes O and LSE directly
+    e = D == 64 ? launch<64, false>(tq, tk, tv, p, grid, s) : launch<128, false>(tq, tk, tv, p, grid, s);
+  } else {
+    e = D == 64 ? launch<64, false, true>(tq, tk, tv, p, grid, s)
+                : launch<128, false, true>(tq, tk, tv, p, grid, s);
+    if (e == cudaSuccess) {
+      const long long rows = (long long)BH * Nq;
+      const unsigned int blocks = (unsigned int)((rows + kCombineWarps - 1) / kCombineWarps);
+      if (D == 64)
+        tk_attn_combine_kernel<64><<<blocks, kCombineWarps * 32, 0, s>>>(
+            p.o_part, p.lse_part, p.o, p.lse, S, rows);
+      else
+        tk_attn_combine_kernel<128><<<blocks, kCombineWarps * 32, 0, s>>>(
+            p.o_part, p.lse_part, p.o, p.lse, S, rows);
+      e = cudaGetLastError();
+    }
+  }
   return e == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 

@@ -65,12 +65,22 @@ struct FwdParams {
   float *lse;        // [BH, N]
   int *err;          // device error word
   int BH;            // batch * heads
-  int N;             // sequence length
+  int N;             // query rows per slice (Nq)
+  int Nk;            // keys per slice (== N except for the split-key call)
   int num_mblocks;   // ceil(N / 256)
   int num_units;     // BH * num_mblocks
   float scale_log2;  // scale * log2(e)
   int test_drop_load;  // test hook: CTA 0 skips its first K load (0 = off)
   int head_group;      // causal unit order: heads per section (>= 1)
+  // Split over keys (inference shape, unmasked): every (slice, 256-query
+  // block) is cut into num_splits ranges of split_tiles 128-key tiles; a unit
+  // writes its range's O / l (fp32) and natural-log LSE to o_part
+  // [num_splits, BH, N, D] and lse_part [num_splits, BH, N], which a second
+  // kernel combines.
+  int num_splits;
+  int split_tiles;
+  float *o_part;
+  float *lse_part;
 };
 
 // Causal units differ in length (a query block visits only the keys up to
@@ -172,7 +182,7 @@ __host__ __device__ __forceinline__ void unit_coords(const FwdParams &p, bool ca
 
 // Number of 128-key tiles Q tile t of block mb visits.
 __host__ __device__ __forceinline__ int kv_tiles(const FwdParams &p, bool causal, int mb, int t) {
-  const int nkv = (p.N + 127) / 128;
+  const int nkv = (p.Nk + 127) / 128;
   if (!causal) return nkv;
   const int last_row = min(mb * 256 + t * 128 + 127, p.N - 1);
   return last_row / 128 + 1;
@@ -190,6 +200,28 @@ __device__ __forceinline__ int unit_at(const SchedFor<kCausal> &tab, const FwdPa
   }
   const int u = blockIdx.x + uc * (int)gridDim.x;
   return u < p.num_units ? u : -1;
+}
+
+// Unit u -> slice, query block, key split and its key tiles: the first tile
+// j0 and how many tiles Q tile 0 / Q tile 1 visit.
+template <bool kCausal, bool kSplit>
+__device__ __forceinline__ void unit_info(const FwdParams &p, int u, int &bh, int &mb, int &s,
+                                          int &j0, int &n0, int &n1) {
+  if constexpr (kSplit) {
+    const int per_bh = p.num_mblocks * p.num_splits;
+    bh = u / per_bh;
+    const int r = u - bh * per_bh;
+    mb = r / p.num_splits;
+    s = r - mb * p.num_splits;
+    j0 = s * p.split_tiles;
+    n0 = n1 = min(p.split_tiles, (p.Nk + 127) / 128 - j0);
+  } else {
+    unit_coords(p, kCausal, u, bh, mb);
+    s = 0;
+    j0 = 0;
+    n0 = kv_tiles(p, kCausal, mb, 0);
+    n1 = kv_tiles(p, kCausal, mb, 1);
+  }
 }
 
 // S = Q K^T for one Q tile: 16 head-dim columns (32 B of a swizzled row) per MMA.
@@ -212,7 +244,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
   for (int kk = 1; kk < 8; ++kk) umma_ts_w<1>(tO, tP + kk * 8, v_lo + kk * (2048 >> 4), dhi, idO);
 }
 
-template <int D, bool kCausal>
+template <int D, bool kCausal, bool kSplit>
 __global__ void __launch_bounds__(512, 1)
     tk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -288,11 +320,9 @@ __global__ void __launch_bounds__(512, 1)
     for (int uc = 0;; ++uc) {
       const int u = unit_at<kCausal>(tab, p, uc);
       if (u < 0) break;
-      int bh, mb;
-      unit_coords(p, kCausal, u, bh, mb);
-      const int n_t = kv_tiles(p, kCausal, mb, t);
-      const int n0 = kv_tiles(p, kCausal, mb, 0);
-      const int n1 = kv_tiles(p, kCausal, mb, 1);
+      int bh, mb, sp, j0, n0, n1;
+      unit_info<kCausal, kSplit>(p, u, bh, mb, sp, j0, n0, n1);
+      const int n_t = t ? n1 : n0;
       const int qrow = mb * 256 + t * 128 + row;  // global query index
       float m_run = -INFINITY, l_run = 0.f;
       int e_cur = 0;  // V exponent O is accumulated at
@@ -318,10 +348,10 @@ __global__ void __launch_bounds__(512, 1)
           if (lane == 0) mbar_arrive(&sb.s_free[t]);
         }
         // Mask keys beyond N, and keys after the query under the causal mask.
-        const int k0 = j * 128;
-        const bool need_mask = (k0 + 128 > p.N) || (kCausal && k0 + 127 > mb * 256 + t * 128);
+        const int k0 = (j0 + j) * 128;
+        const bool need_mask = (k0 + 128 > p.Nk) || (kCausal && k0 + 127 > mb * 256 + t * 128);
         if (need_mask) {
-          int lim = p.N - k0;
+          int lim = p.Nk - k0;
           if (kCausal) lim = min(lim, qrow - k0 + 1);
 #pragma unroll
           for (int i = 0; i < 128; ++i)
@@ -472,16 +502,12 @@ __global__ void __launch_bounds__(512, 1)
     uint32_t kvb = 0;
     uint32_t conv_count = 0;  // V tiles converted (conv_bar phases)
     // the unit whose epilogue is pending
-    int pend_bh = -1, pend_mb = 0, pend_uc = 0, pend_e[2] = {0, 0};
+    int pend_bh = -1, pend_mb = 0, pend_sp = 0, pend_uc = 0, pend_e[2] = {0, 0};
     for (int uc = 0;; ++uc) {
       const int u = unit_at<kCausal>(tab, p, uc);
       const bool have_unit = u >= 0;
-      int bh = 0, mb = 0, n0 = 0, n1 = 0;
-      if (have_unit) {
-        unit_coords(p, kCausal, u, bh, mb);
-        n0 = kv_tiles(p, kCausal, mb, 0);
-        n1 = kv_tiles(p, kCausal, mb, 1);
-      }
+      int bh = 0, mb = 0, sp = 0, j0 = 0, n0 = 0, n1 = 0;
+      if (have_unit) unit_info<kCausal, kSplit>(p, u, bh, mb, sp, j0, n0, n1);
       int e_run = 0, e_t0 = 0, e_t1 = 0;
       for (int j = 0; j <= n1; ++j) {
         // The previous unit's epilogue runs after this unit's first V tile
@@ -502,30 +528,53 @@ __global__ void __launch_bounds__(512, 1)
             const float oscale = exp2i(-pend_e[t]) / l;
             const int qrow = pend_mb * 256 + t * 128 + row;
             const bool valid = qrow < p.N;
-            __nv_bfloat16 *orow = p.o + ((size_t)pend_bh * p.N + (valid ? qrow : 0)) * D;
             const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
+            if constexpr (kSplit) {
+              // this key range's O / l in fp32, and its LSE, for the combine
+              const size_t prow = ((size_t)pend_sp * p.BH + pend_bh) * p.N + (valid ? qrow : 0);
+              float4 *orow = reinterpret_cast<float4 *>(p.o_part + prow * D);
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t r[32];
-              tmem_ld_32x32b_x32(tO + c0, r);
-              tmem_wait_ld();
-              uint32_t pk[16];
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tO + c0, r);
+                tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                reg_barrier(r[2 * i]);
-                reg_barrier(r[2 * i + 1]);
-                pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * oscale,
-                                    __uint_as_float(r[2 * i + 1]) * oscale);
-              }
-              if (valid) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+                for (int i = 0; i < 32; ++i) reg_barrier(r[i]);
+                if (valid) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                  for (int i = 0; i < 8; ++i)
+                    orow[c0 / 4 + i] = make_float4(__uint_as_float(r[4 * i]) * oscale,
+                                                   __uint_as_float(r[4 * i + 1]) * oscale,
+                                                   __uint_as_float(r[4 * i + 2]) * oscale,
+                                                   __uint_as_float(r[4 * i + 3]) * oscale);
+                }
               }
+              if (valid) p.lse_part[prow] = (m + lg2_approx(l)) * 0.69314718055994531f;
+            } else {
+              __nv_bfloat16 *orow = p.o + ((size_t)pend_bh * p.N + (valid ? qrow : 0)) * D;
+#pragma unroll 1
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tO + c0, r);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  reg_barrier(r[2 * i]);
+                  reg_barrier(r[2 * i + 1]);
+                  pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * oscale,
+                                      __uint_as_float(r[2 * i + 1]) * oscale);
+                }
+                if (valid) {
+                  uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+              }
+              if (valid)
+                p.lse[(size_t)pend_bh * p.N + qrow] = (m + lg2_approx(l)) * 0.69314718055994531f;
             }
-            if (valid)
-              p.lse[(size_t)pend_bh * p.N + qrow] = (m + lg2_approx(l)) * 0.69314718055994531f;
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sb.o_free[t]);
@@ -621,6 +670,7 @@ __global__ void __launch_bounds__(512, 1)
       if (!have_unit) break;
       pend_bh = bh;
       pend_mb = mb;
+      pend_sp = sp;
       pend_uc = uc;
       pend_e[0] = e_t0;
       pend_e[1] = e_t1;
@@ -656,10 +706,9 @@ __global__ void __launch_bounds__(512, 1)
         for (int uc = 0;; ++uc) {
           const int u = unit_at<kCausal>(tab, p, uc);
           if (u < 0) break;
-          int bh, mb;
-          unit_coords(p, kCausal, u, bh, mb);
-          const int n1 = kv_tiles(p, kCausal, mb, 1);
-          const int n_t = t ? n1 : kv_tiles(p, kCausal, mb, 0);
+          int bh, mb, sp, j0, n0, n1;
+          unit_info<kCausal, kSplit>(p, u, bh, mb, sp, j0, n0, n1);
+          const int n_t = t ? n1 : n0;
           const int qb = uc % C::kQBufs;  // Q buffer of this unit
 #pragma unroll 1
           for (int j = 0; j <= n1; ++j) {
@@ -732,10 +781,8 @@ __global__ void __launch_bounds__(512, 1)
       for (int uc = 0;; ++uc) {
         const int u = unit_at<kCausal>(tab, p, uc);
         if (u < 0) break;
-        int bh, mb;
-        unit_coords(p, kCausal, u, bh, mb);
-        const int n0 = kv_tiles(p, kCausal, mb, 0);
-        const int n1 = kv_tiles(p, kCausal, mb, 1);
+        int bh, mb, sp, j0, n0, n1;
+        unit_info<kCausal, kSplit>(p, u, bh, mb, sp, j0, n0, n1);
 #pragma unroll 1
         for (int j = 0; j <= n1; ++j) {
           const uint32_t kidx = kvb + 2 * j, vidx = kidx - 1;  // K_j and V_{j-1}
@@ -816,9 +863,8 @@ __global__ void __launch_bounds__(512, 1)
       for (int uc = 0;; ++uc) {
         const int u = unit_at<kCausal>(tab, p, uc);
         if (u < 0) break;
-        int bh, mb;
-        unit_coords(p, kCausal, u, bh, mb);
-        const int n1 = kv_tiles(p, kCausal, mb, 1);
+        int bh, mb, sp, j0, n0, n1;
+        unit_info<kCausal, kSplit>(p, u, bh, mb, sp, j0, n0, n1);
         // Q buffer qb was last used kQBufs units ago
         const int qb = uc % C::kQBufs;
         if (uc >= C::kQBufs && !mbar_wait(&sb.q_empty[qb], (uc / C::kQBufs - 1) & 1, abort_flag)) {
@@ -851,7 +897,7 @@ __global__ void __launch_bounds__(512, 1)
             const CUtensorMap *tm = kv ? &tm_v : &tm_k;
             for (int ch = 0; ch < C::kChunks; ++ch)
               tma_load_3d_hint(sKV + s * C::kTileBytes + ch * C::kChunkBytes, tm, &sb.kv_full[s],
-                               ch * 64, j * 128, bh, pol_kv);
+                               ch * 64, (j0 + j) * 128, bh, pol_kv);
             ++kv_idx;
           }
         }

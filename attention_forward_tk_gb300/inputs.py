@@ -14,11 +14,17 @@ Workloads (the five problem shapes the library is measured and checked on):
   n16384_d128_c   4   32  16384  128  causal   Q, K ~ 4 N(0, 1);
                                                V ~ Student-t(3), clipped to +-8
 
+and one inference shape, queries and keys of different lengths (timed beside
+them, split over keys):
+
+  prefill_q256_k32k_d128  B 1, H 32, Nq 256, Nk 32768, D 128, unmasked, N(0, 1)
+
 The scale is 1/sqrt(D) in every workload (the kernel examples on the pages use
 1/sqrt(64) = 0.125 and 1/sqrt(128) ~= 0.08838834764).
 
-Recipe: a CPU ``torch.Generator`` seeded with the workload's index (0..4) draws
-Q, then K, then V, in float32, with the shape [B, H, N, D]; scaling (4 N(0,1))
+Recipe: a CPU ``torch.Generator`` seeded with the workload's index (0..5) draws
+Q, then K, then V, in float32, with the shape [B, H, N, D] (K and V [B, H, Nk,
+D] for the inference shape); scaling (4 N(0,1))
 and clipping happen in float32 before one round-to-nearest-even conversion to
 bfloat16.  A Student-t(3) draw is z / sqrt((z1^2 + z2^2 + z3^2) / 3) with all
 four normals from the same generator (z first, then a [..., 3] block).
@@ -41,6 +47,11 @@ class Workload:
     causal: bool
     dist: str  # "normal" or "peaky_t3"
     seed: int
+    Nk: int = 0  # keys per slice when it differs from N (inference shape, unmasked)
+
+    @property
+    def keys(self) -> int:
+        return self.Nk or self.N
 
     @property
     def scale(self) -> float:
@@ -51,16 +62,22 @@ class Workload:
         return (self.B, self.H, self.N, self.D)
 
     @property
+    def kv_shape(self):
+        return (self.B, self.H, self.keys, self.D)
+
+    @property
     def flops(self) -> float:
-        """4*B*H*N^2*D, halved under the causal mask."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.D
+        """4*B*H*N*Nk*D (Nk = N but for the inference shape), halved under the
+        causal mask."""
+        f = 4.0 * self.B * self.H * self.N * self.keys * self.D
         return f / 2 if self.causal else f
 
     @property
     def io_bytes(self) -> int:
         """Q, K, V read and O written in bf16, LSE written in fp32."""
-        elems = self.B * self.H * self.N * self.D
-        return 4 * elems * 2 + self.B * self.H * self.N * 4
+        q_elems = self.B * self.H * self.N * self.D
+        kv_elems = self.B * self.H * self.keys * self.D
+        return (2 * q_elems + 2 * kv_elems) * 2 + self.B * self.H * self.N * 4
 
 
 WORKLOADS = (
@@ -70,7 +87,13 @@ WORKLOADS = (
     Workload("n8192_d128_c", 8, 16, 8192, 128, True, "normal", 3),
     Workload("n16384_d128_c", 4, 32, 16384, 128, True, "peaky_t3", 4),
 )
-BY_NAME = {w.name: w for w in WORKLOADS}
+# The inference shape (a split over keys, tk_attn_fwd_splitkv): a 256-query
+# prefill chunk of 32 heads against 32768 cached keys, unmasked.  Not one of
+# the five measured configurations; timed beside them.
+EXTRA_WORKLOADS = (
+    Workload("prefill_q256_k32k_d128", 1, 32, 256, 128, False, "normal", 5, Nk=32768),
+)
+BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 
 
 def _randn(g: torch.Generator, shape) -> torch.Tensor:
@@ -84,7 +107,7 @@ def _student_t3(g: torch.Generator, shape) -> torch.Tensor:
     return z / torch.sqrt(chi2_over_nu)
 
 
-def draw(shape, seed: int, dist: str = "normal", device="cpu"):
+def draw(shape, seed: int, dist: str = "normal", device="cpu", kv_shape=None):
     """Q, K, V as bf16 tensors of `shape`, per the recipe above.
 
     With the default CPU generator the values are the ones every parity test
@@ -92,20 +115,21 @@ def draw(shape, seed: int, dist: str = "normal", device="cpu"):
     the device's generator (other values, no host work): the benchmark uses
     it for full-size inputs it does not compare.
     """
+    kvs = shape if kv_shape is None else kv_shape
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
     if dist == "normal":
         q = _randn(g, shape)
-        k = _randn(g, shape)
-        v = _randn(g, shape)
+        k = _randn(g, kvs)
+        v = _randn(g, kvs)
     elif dist == "peaky_t3":
         q = 4.0 * _randn(g, shape)
-        k = 4.0 * _randn(g, shape)
-        v = _student_t3(g, shape).clamp_(-8.0, 8.0)
+        k = 4.0 * _randn(g, kvs)
+        v = _student_t3(g, kvs).clamp_(-8.0, 8.0)
     else:
         raise ValueError(f"unknown distribution {dist!r}")
     return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
 
 
 def workload_inputs(w: Workload, device="cpu"):
-    return draw(w.shape, w.seed, w.dist, device=device)
+    return draw(w.shape, w.seed, w.dist, device=device, kv_shape=w.kv_shape)

@@ -180,18 +180,23 @@ def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
 
     def row_flops(rows):
         i = rows % w.N
-        keys = (i + 1) if w.causal else np.full_like(i, w.N)
+        keys = (i + 1) if w.causal else np.full_like(i, w.keys)
         return float((4.0 * w.D * keys).sum())
+
+    def oracle_rows(rows):
+        if w.Nk:
+            return oracle.attention_qk_rows(q, k, v, w.scale, w.causal, rows)
+        return oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
 
     # calibrate on a small batch, then run one batch sized to the budget
     rows = rng.integers(0, BH * w.N, size=64)
     t0 = time.perf_counter()
-    _, _, threads = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    _, _, threads = oracle_rows(rows)
     dt = max(time.perf_counter() - t0, 1e-4)
     n = int(min(BH * w.N, max(64, 64 * budget_s / dt)))
     rows = rng.integers(0, BH * w.N, size=n)
     t0 = time.perf_counter()
-    _, _, threads = oracle.attention_rows(q, k, v, w.scale, w.causal, rows)
+    _, _, threads = oracle_rows(rows)
     dt = time.perf_counter() - t0
     return row_flops(rows) / dt / 1e12, threads, n, dt
 
@@ -212,11 +217,22 @@ def time_gpu(w, steps: int, warmup: int, device):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     sh = stream.cuda_stream
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-            w.B, w.H, w.N, w.D, w.scale, int(w.causal), sh)
+    if w.Nk:
+        # inference shape: the split-over-keys call, default split count
+        need = api.tk_attn_splitkv_workspace_bytes(w.B, w.H, w.N, w.Nk, w.D, 0)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                w.B, w.H, w.N, w.Nk, w.D, w.scale, 0, ws.data_ptr(), need, sh)
+        call = api.tk_attn_fwd_splitkv
+        per_call = 2 if need > 0 else 1  # the ranges kernel, then the combine kernel
+    else:
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                w.B, w.H, w.N, w.D, w.scale, int(w.causal), sh)
+        call = api.tk_attn_fwd
+        per_call = 1
     for _ in range(warmup):
         flush.zero_()
-        st = api.tk_attn_fwd(*args)
+        st = call(*args)
         if st:
             raise RuntimeError(api.tk_attn_status_string(st))
     if api.tk_attn_last_device_error(sh) != 0:
@@ -228,14 +244,14 @@ def time_gpu(w, steps: int, warmup: int, device):
     for a, b in evs:
         flush.zero_()
         a.record(stream)
-        api.tk_attn_fwd(*args)
+        call(*args)
         b.record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
     if api.tk_attn_last_device_error(sh) != 0:
         raise RuntimeError("device-side barrier timeout during timing")
     ms = [a.elapsed_time(b) for a, b in evs]
-    return ms, wall, steps
+    return ms, wall, steps * per_call
 
 
 def time_e2e(w, steps: int, warmup: int, device):
@@ -252,18 +268,37 @@ def time_e2e(w, steps: int, warmup: int, device):
             torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device))
     o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, pin_memory=True)
+    if w.Nk:
+        # inference shape: copies in, the split-over-keys call, copies out
+        from attention_forward_tk_gb300 import attention_forward_splitkv
+        from attention_forward_tk_gb300.api import tk_attn_splitkv_workspace_bytes
+        need = tk_attn_splitkv_workspace_bytes(w.B, w.H, w.N, w.Nk, w.D, 0)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+
+        def step():
+            qd, kd, vd, od, ld = bufs
+            qd.copy_(q, non_blocking=True)
+            kd.copy_(k, non_blocking=True)
+            vd.copy_(v, non_blocking=True)
+            attention_forward_splitkv(qd, kd, vd, w.scale, 0, od, ld, ws)
+            o.copy_(od, non_blocking=True)
+            lse.copy_(ld, non_blocking=True)
+            torch.cuda.current_stream(device).synchronize()
+    else:
+        def step():
+            attention_forward_host(q, k, v, w.causal, w.scale, bufs, o, lse)
     for _ in range(warmup):
-        attention_forward_host(q, k, v, w.causal, w.scale, bufs, o, lse)
+        step()
     stream = torch.cuda.current_stream(device)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(device)
     a.record(stream)
     for _ in range(steps):
-        attention_forward_host(q, k, v, w.causal, w.scale, bufs, o, lse)
+        step()
     b.record(stream)
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(b) / steps
-    h2d = 3 * q.numel() * 2
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = o.numel() * 2 + lse.numel() * 4
     return ms, h2d, d2h
 
@@ -289,7 +324,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from attention_forward_tk_gb300.inputs import BY_NAME, WORKLOADS
+    from attention_forward_tk_gb300.inputs import BY_NAME, EXTRA_WORKLOADS, WORKLOADS
     w = BY_NAME[args.workload]
     world, rank, local = dist_env()
 
@@ -335,7 +370,7 @@ def main():
 
     extra = {}
     if args.all_workloads:
-        for ow in WORKLOADS:
+        for ow in WORKLOADS + EXTRA_WORKLOADS:
             # enough launches for about half a second, so the clock sampler
             # sees the workload run
             probe, _, _ = time_gpu(ow, 3, 3, device)
@@ -355,6 +390,10 @@ def main():
 
     peak_tf, peak_hbm, peak_kind = measured_peaks()
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    hbm_gbs = w.io_bytes / (kernel_ms / 1e3) / 1e9
+    # the binding roofline: the tensor cores, unless moving the algorithmic
+    # bytes at the HBM peak takes longer than the flops at the tensor peak
+    hbm_bound = w.io_bytes / (peak_hbm * 1e9) > w.flops / (peak_tf * 1e12)
     traffic = recorded_traffic(w.name)
     line = {
         "metric": "attention fwd TFLOP/s (bf16, 1xGB300) and % of dense BF16 tensor peak",
@@ -369,18 +408,23 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.keys, "D": w.D,
                    "causal": w.causal, "values": w.dist, "flops_per_step": w.flops,
                    "l2": "flushed (256 MB write) before every timed step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
-                     "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_tf, 4),
-                     "peak_kind": f"{peak_kind} dense bf16 (burst)",
-                     "traffic": traffic,
-                     "algorithmic_bytes": w.io_bytes,
-                     "hbm_gbs": round(w.io_bytes / (kernel_ms / 1e3) / 1e9, 1),
-                     "hbm_peak_gbs": peak_hbm},
+        "roofline": ({"bound": "hbm", "achieved": round(hbm_gbs, 1),
+                      "peak": peak_hbm, "unit": "GB/s",
+                      "frac": round(hbm_gbs / peak_hbm, 4),
+                      "peak_kind": f"{peak_kind} HBM copy",
+                      "tensor_tflops": round(achieved, 1),
+                      "tensor_frac": round(achieved / peak_tf, 4)}
+                     if hbm_bound else
+                     {"bound": "tensor", "achieved": round(achieved, 1),
+                      "peak": peak_tf, "unit": "TFLOP/s",
+                      "frac": round(achieved / peak_tf, 4),
+                      "peak_kind": f"{peak_kind} dense bf16 (burst)",
+                      "hbm_gbs": round(hbm_gbs, 1),
+                      "hbm_peak_gbs": peak_hbm}),
         "e2e": None if args.no_e2e else {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
@@ -389,6 +433,8 @@ def main():
         "kernel_ms_median": round(statistics.median(ms), 5),
         "clocks": clk.summary(),
     }
+    line["roofline"]["traffic"] = traffic
+    line["roofline"]["algorithmic_bytes"] = w.io_bytes
     if extra:
         line["all_workloads"] = extra
     if not args.no_cpu_baseline and world >= 1:
@@ -422,7 +468,7 @@ def main_reference(args, w, world, rank):
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.keys, "D": w.D,
                    "causal": w.causal, "values": w.dist, "flops_per_step": w.flops},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{samples[0][1]} random rows of {w.name} per step "

@@ -39,6 +39,8 @@
 #ifndef TK_ATTN_H_
 #define TK_ATTN_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -57,7 +59,7 @@ typedef struct CUstream_st *tk_attn_stream_t;
                                            barrier (reported by
                                            tk_attn_last_device_error only) */
 
-#define TK_ATTN_VERSION 10000 /* major*10000 + minor*100 + patch */
+#define TK_ATTN_VERSION 10100 /* major*10000 + minor*100 + patch */
 
 /*
  * tk_attn_fwd -- fused attention forward, asynchronous on `stream`.
@@ -89,6 +91,52 @@ int tk_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse
 int tk_attn_check_args(const void *q, const void *k, const void *v, const void *o,
                        const float *lse, int B, int H, int N, int D, float scale,
                        int causal);
+
+/*
+ * tk_attn_fwd_splitkv -- the same attention for Nq query rows against Nk
+ * keys per (batch, head) slice, unmasked, with the keys split into ranges
+ * processed in parallel: the inference shape (a block of new queries against
+ * a long run of cached keys), where (slice, 256-query block) pairs alone
+ * would leave most SMs idle.  Every key is visible to every query.
+ *
+ * Definition: the attention definition of the flash-attention examples in
+ * the ThunderKittens news write-up (88811315.cn, post 77732), with the query
+ * and key counts apart.  The split is exact: range s yields O_s (normalised
+ * by its own row sum) and LSE_s, and LSE = ln sum_s exp(LSE_s),
+ * O = sum_s exp(LSE_s - LSE) O_s, the same deferred normalisation the
+ * examples' per-tile loop applies between K/V tiles.  The pages give no
+ * separate inference kernel; this is the plain reading of attention at
+ * inference.
+ *
+ * Arguments (device pointers, contiguous, row-major, 16-byte aligned):
+ *   q, o        bf16 [B, H, Nq, D];  k, v  bf16 [B, H, Nk, D];  lse  fp32 [B, H, Nq]
+ *   num_splits  key ranges; <= 0 picks enough ranges that (slice, query block,
+ *               range) units cover every SM.  Clamped to one range per
+ *               128-key tile, and to a count that leaves no range empty.
+ *   workspace   device memory the caller owns, at least
+ *               tk_attn_splitkv_workspace_bytes(...) bytes (0 when the call
+ *               uses one range; then workspace may be NULL); 16-byte aligned,
+ *               disjoint from the tensors.  Holds per-range O_s (fp32) and
+ *               LSE_s.  Calls that share a workspace must not overlap on the
+ *               GPU.
+ *   D, scale, stream as for tk_attn_fwd.
+ * Two kernel launches on `stream` (ranges, then their combination), or one
+ * when there is a single range.  Allocates nothing.
+ * Returns TK_ATTN_OK, _INVALID_ARG (null or overlapping pointers, sizes <= 0,
+ * bad scale, missing or short workspace), _UNSUPPORTED (head dim, alignment,
+ * sizes), _ARCH or _LAUNCH; outputs are untouched on any error.
+ */
+int tk_attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int B, int H, int Nq, int Nk, int D, float scale, int num_splits,
+                        void *workspace, size_t workspace_bytes, tk_attn_stream_t stream);
+
+/*
+ * tk_attn_splitkv_workspace_bytes -- workspace tk_attn_fwd_splitkv needs for
+ * these sizes and split request on the current device (the default split
+ * count depends on its SM count): S * B * H * Nq * (D + 1) * 4 bytes for S
+ * ranges, 0 for one range or for invalid sizes.
+ */
+size_t tk_attn_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int D, int num_splits);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char *tk_attn_status_string(int status);

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol(tk_lib):
 
 
 def test_version_and_status_strings(tk_lib):
-    assert tk_lib.tk_attn_version() == 10000
+    assert tk_lib.tk_attn_version() == 10100
     for code in (0, -1, -2, -3, -4, -5):
         s = tk_lib.tk_attn_status_string(code)
         assert s and s != "unknown status"
@@ -94,3 +94,28 @@ def test_binding_raises_when_library_missing(monkeypatch):
     monkeypatch.setattr(api, "LIB_PATH", "/nonexistent/libtk_attn.so")
     with pytest.raises(api.TkAttnError):
         api.library()
+
+
+def test_splitkv_rejects_bad_arguments_before_touching_cuda(tk_lib):
+    # the argument checks of the split-key call run before any CUDA call
+    args = dict(B=1, H=2, Nq=16, Nk=300, D=64, scale=0.125, splits=0)
+
+    def call(q=Q, k=K, v=V, o=O, lse=L, **kw):
+        a = dict(args, **kw)
+        return tk_lib.tk_attn_fwd_splitkv(q, k, v, o, lse, a["B"], a["H"], a["Nq"], a["Nk"],
+                                          a["D"], a["scale"], a["splits"], 0, 0, 0)
+    assert call(q=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert call(Nk=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert call(scale=-1.0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert call(D=96) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    assert call(k=K + 8) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    # O [1,2,16,64] bf16 = 4096 bytes: LSE inside it overlaps
+    assert call(lse=O + 1024) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+
+
+def test_splitkv_workspace_query_without_a_gpu(tk_lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert tk_lib.tk_attn_splitkv_workspace_bytes(1, 2, 16, 300, 64, 4) == 0
+    assert tk_lib.tk_attn_splitkv_workspace_bytes(1, 2, 16, 300, 96, 4) == 0

@@ -1,0 +1,111 @@
+"""Queries and keys of different lengths with the keys split into ranges
+(tk_attn_fwd_splitkv), through the C ABI, against the fp64 oracle's
+attention_qk, element by element.  Tolerances as for the single-pass call:
+max |dO| <= 2e-2, mean |dO| <= 2e-3, max |dLSE| <= 1e-3."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import TOL_LSE_MAX, TOL_O_MAX, TOL_O_MEAN
+
+pytestmark = pytest.mark.gpu
+
+
+def draw_qk(B, H, Nq, Nk, D, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, Nq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H, Nk, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, Nk, D), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+def run_split(tk_lib, q, k, v, scale, splits, ws_extra=0, ws_bytes=None):
+    dev = torch.device("cuda", 0)
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device=dev)
+    need = tk_lib.tk_attn_splitkv_workspace_bytes(B, H, Nq, Nk, D, splits)
+    ws = torch.empty(max(need + ws_extra, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = tk_lib.tk_attn_fwd_splitkv(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), B, H, Nq, Nk, D, scale, splits,
+                                    ws.data_ptr(), need if ws_bytes is None else ws_bytes, stream)
+    if st != 0:
+        torch.cuda.synchronize()
+        return st, o, lse, need
+    assert tk_lib.tk_attn_last_device_error(stream) == 0
+    torch.cuda.synchronize()
+    return st, o.float().cpu().double().numpy(), lse.cpu().double().numpy(), need
+
+
+CASES = [
+    # (B, H, Nq, Nk, D, splits)
+    (1, 4, 256, 4096, 128, 0),   # default split count (one 128-key tile per range here)
+    (2, 3, 100, 3000, 64, 5),    # ragged query and key tails
+    (1, 8, 1, 2048, 128, 0),     # one query row per slice (decode)
+    (1, 2, 300, 1000, 64, 1),    # one range: the single-pass kernel with Nq != Nk
+    (1, 1, 17, 129, 128, 7),     # 2 key tiles: clamped to 2 ranges
+    (2, 2, 512, 256, 64, 0),     # more queries than keys
+    (1, 2, 640, 5000, 128, 3),   # 3 query blocks x 3 ranges
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_splitkv_parity(tk_lib, oracle_lib, case):
+    B, H, Nq, Nk, D, splits = case
+    q, k, v = draw_qk(B, H, Nq, Nk, D, seed=500 + Nq + Nk + D + splits)
+    scale = 1 / math.sqrt(D)
+    st, o, lse, _ = run_split(tk_lib, q, k, v, scale, splits)
+    assert st == 0, tk_lib.tk_attn_status_string(st)
+    o_ref, lse_ref = oracle_lib.attention_qk(q, k, v, scale, False)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    do = np.abs(o - o_ref)
+    assert do.max() <= TOL_O_MAX, do.max()
+    assert do.mean() <= TOL_O_MEAN, do.mean()
+    assert np.abs(lse - lse_ref).max() <= TOL_LSE_MAX
+
+
+def test_splitkv_ranges_agree_with_one_range(tk_lib):
+    # the combination over ranges against the single-pass result: both within
+    # rounding of one another for every split count
+    q, k, v = draw_qk(1, 4, 256, 2048, 64, seed=601)
+    _, o1, l1, need1 = run_split(tk_lib, q, k, v, 0.125, 1)
+    assert need1 == 0
+    for s in (2, 3, 16):
+        st, o, l, need = run_split(tk_lib, q, k, v, 0.125, s)
+        assert st == 0 and need > 0
+        assert np.abs(o - o1).max() <= 2e-2
+        assert np.abs(l - l1).max() <= 1e-4
+
+
+def test_splitkv_rejects_a_short_workspace(tk_lib):
+    q, k, v = draw_qk(1, 2, 128, 1024, 128, seed=602)
+    B, H, Nq, Nk, D = 1, 2, 128, 1024, 128
+    need = tk_lib.tk_attn_splitkv_workspace_bytes(B, H, Nq, Nk, D, 4)
+    assert need == 4 * B * H * Nq * (D + 1) * 4
+    st, o, lse, _ = run_split(tk_lib, q, k, v, 0.1, 4, ws_bytes=need - 16)
+    assert st == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert torch.isnan(o).all() and torch.isnan(lse).all()  # outputs untouched
+
+
+def test_inference_workload_sampled_rows(tk_lib, oracle_lib):
+    # the timed inference shape at full size (B1 H32 Nq256 Nk32768 D128, the
+    # default split count), checked on rows spread over the heads
+    from attention_forward_tk_gb300.inputs import BY_NAME, workload_inputs
+    w = BY_NAME["prefill_q256_k32k_d128"]
+    q, k, v = workload_inputs(w)
+    st, o, lse, need = run_split(tk_lib, q, k, v, w.scale, 0)
+    assert st == 0 and need > 0
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, w.H * w.N - 1],
+                                     rng.integers(0, w.B * w.H * w.N, 120)]))
+    o_ref, lse_ref, _ = oracle_lib.attention_qk_rows(q, k, v, w.scale, False, rows)
+    of = o.reshape(-1, w.D)[rows]
+    lf = lse.reshape(-1)[rows]
+    assert np.abs(of - o_ref).max() <= TOL_O_MAX
+    assert np.abs(of - o_ref).mean() <= TOL_O_MEAN
+    assert np.abs(lf - lse_ref).max() <= TOL_LSE_MAX
