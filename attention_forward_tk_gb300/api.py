@@ -26,11 +26,13 @@ TK_ATTN_ERR_UNSUPPORTED = -2
 TK_ATTN_ERR_ARCH = -3
 TK_ATTN_ERR_LAUNCH = -4
 TK_ATTN_ERR_DEVICE_TIMEOUT = -5
+TK_ATTN_ERR_TOO_LARGE = -6
 
 # every symbol include/tk_attn.h declares
 EXPORTED = (
     "tk_attn_fwd",
     "tk_attn_fwd_splitkv",
+    "tk_attn_fwd_splitkv_static",
     "tk_attn_splitkv_workspace_bytes",
     "tk_attn_check_args",
     "tk_attn_status_string",
@@ -72,6 +74,8 @@ def library() -> ctypes.CDLL:
         lib.tk_attn_fwd_splitkv.restype = i
         lib.tk_attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
                                             ctypes.c_size_t, vp]
+        lib.tk_attn_fwd_splitkv_static.restype = i
+        lib.tk_attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.tk_attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.tk_attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.tk_attn_check_args.restype = i
@@ -103,6 +107,14 @@ def tk_attn_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int
     return int(library().tk_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, D,
                                              ctypes.c_float(scale), int(num_splits), workspace,
                                              int(workspace_bytes), stream))
+
+
+def tk_attn_fwd_splitkv_static(q: int, k: int, v: int, o: int, lse: int, B: int, H: int,
+                               Nq: int, Nk: int, D: int, scale: float, num_splits: int,
+                               stream: int) -> int:
+    return int(library().tk_attn_fwd_splitkv_static(q, k, v, o, lse, B, H, Nq, Nk, D,
+                                                    ctypes.c_float(scale), int(num_splits),
+                                                    stream))
 
 
 def tk_attn_splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, D: int,

@@ -25,6 +25,13 @@ namespace {
 // Device error word: kernels record a bounded wait that ran out here.
 __device__ int g_dev_error;
 
+// Scratch of the no-allocation split-over-keys entry point: the per-range
+// partial O (fp32) and LSE.  Every device that loads the library holds it
+// until the process exits.  Host code must not take its name for a device
+// address: the address comes from cudaGetSymbolAddress at per-device set-up.
+constexpr size_t kStaticScratchBytes = 64ull << 20;
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kStaticScratchBytes];
+
 constexpr int kMaxDevices = 64;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -37,6 +44,7 @@ struct DeviceState {
   int status = TK_ATTN_ERR_ARCH;
   int num_sms = 0;
   int *err_word = nullptr;  // address of g_dev_error on this device
+  void *static_scratch = nullptr;  // address of g_splitkv_scratch on this device
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -81,6 +89,8 @@ void init_device(int dev, DeviceState &ds) {
                  cudaSuccess)
     st = TK_ATTN_ERR_LAUNCH;
   if (!st && cudaMemset(ds.err_word, 0, sizeof(int)) != cudaSuccess) st = TK_ATTN_ERR_LAUNCH;
+  if (!st && cudaGetSymbolAddress(&ds.static_scratch, g_splitkv_scratch) != cudaSuccess)
+    st = TK_ATTN_ERR_LAUNCH;
   if (!st && cudaDeviceSynchronize() != cudaSuccess) st = TK_ATTN_ERR_LAUNCH;
   ds.status = st;
 }
@@ -427,6 +437,22 @@ extern "C" int tk_attn_fwd_splitkv(const void *q, const void *k, const void *v, 
   return e == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 
+extern "C" int tk_attn_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o,
+                                          float *lse, int B, int H, int Nq, int Nk, int D,
+                                          float scale, int num_splits,
+                                          tk_attn_stream_t stream) {
+  int st = check_splitkv_args(q, k, v, o, lse, B, H, Nq, Nk, D, scale);
+  if (st) return st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  const long long BH = (long long)B * H;
+  int S, T;
+  resolve_splits(num_splits, BH * ((Nq + 255LL) / 256), (Nk + 127) / 128, ds->num_sms, &S, &T);
+  if (split_workspace(BH, Nq, D, S) > kStaticScratchBytes) return TK_ATTN_ERR_TOO_LARGE;
+  return tk_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, D, scale, num_splits,
+                             ds->static_scratch, kStaticScratchBytes, stream);
+}
+
 extern "C" const char *tk_attn_status_string(int status) {
   switch (status) {
     case TK_ATTN_OK: return "ok";
@@ -435,6 +461,9 @@ extern "C" const char *tk_attn_status_string(int status) {
     case TK_ATTN_ERR_ARCH: return "no compute-capability 10.3 GPU current";
     case TK_ATTN_ERR_LAUNCH: return "CUDA error while preparing or launching the kernel";
     case TK_ATTN_ERR_DEVICE_TIMEOUT: return "a kernel abandoned a barrier wait";
+    case TK_ATTN_ERR_TOO_LARGE:
+      return "the split needs more than the 64 MiB static scratch of tk_attn_fwd_splitkv_static "
+             "(use fewer key ranges, or tk_attn_fwd_splitkv with a workspace)";
     default: return "unknown status";
   }
 }

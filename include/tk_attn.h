@@ -58,6 +58,8 @@ typedef struct CUstream_st *tk_attn_stream_t;
 #define TK_ATTN_ERR_DEVICE_TIMEOUT (-5) /* a kernel gave up waiting on an on-chip
                                            barrier (reported by
                                            tk_attn_last_device_error only) */
+#define TK_ATTN_ERR_TOO_LARGE (-6)      /* tk_attn_fwd_splitkv_static: the ranges'
+                                           partial results exceed its static scratch */
 
 #define TK_ATTN_VERSION 10100 /* major*10000 + minor*100 + patch */
 
@@ -137,6 +139,29 @@ int tk_attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, fl
  * ranges, 0 for one range or for invalid sizes.
  */
 size_t tk_attn_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int D, int num_splits);
+
+/*
+ * tk_attn_fwd_splitkv_static -- tk_attn_fwd_splitkv for callers that cannot
+ * allocate device memory: no workspace argument, and the call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).  The
+ * per-range partial results go to a 64 MiB scratch array that is part of
+ * the library (a static device array: every GPU that loads the library holds
+ * it until the process exits).  The pages have no counterpart: this is an
+ * interface variant, not a step of the method.
+ *
+ * Arguments, ranges and results as for tk_attn_fwd_splitkv.  Returns
+ * TK_ATTN_ERR_TOO_LARGE, outputs untouched, when the ranges' partial results
+ * (tk_attn_splitkv_workspace_bytes) exceed 64 MiB; fewer ranges
+ * (num_splits) or the workspace call then serve.  Nothing in the scratch
+ * needs to start at zero.  Every call shares the one array, so calls that
+ * overlap on the GPU (other streams, or other threads) race: serialise them.
+ * The first call of any tk_attn entry point on a device sets the device up
+ * (kernel attributes, the scratch and error-word addresses); make that call
+ * before any stream capture.
+ */
+int tk_attn_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o,
+                               float *lse, int B, int H, int Nq, int Nk, int D, float scale,
+                               int num_splits, tk_attn_stream_t stream);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char *tk_attn_status_string(int status);
