@@ -12,6 +12,8 @@ Contents
   attention_qk_rows, attention_qk
                    the same definition for Nq queries against Nk keys
                    (inference shape); causal aligned to the last key
+  gemm_abt         C = A B^T for bf16 A [M, K], B [N, K] in float64, with the
+                   per-element magnitude sum that bounds fp32 accumulation
   tiled_online_softmax
                    numpy restatement of the tile-by-tile online-softmax
                    recurrence the kernel examples on the pages use, both in
@@ -27,6 +29,7 @@ log over scaled, masked scores).
 """
 from .brute import (attention, attention_qk, attention_qk_rows, attention_rows, build, lib_path,
                     max_threads)
+from .gemm import gemm_abt
 from .tiled import tiled_online_softmax
 
 __all__ = [
@@ -35,6 +38,7 @@ __all__ = [
     "attention_qk_rows",
     "attention_rows",
     "build",
+    "gemm_abt",
     "lib_path",
     "max_threads",
     "tiled_online_softmax",

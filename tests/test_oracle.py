@@ -322,3 +322,46 @@ def test_qk_rejects_causal_with_more_queries_than_keys(oracle_lib):
     q, k, v = qk_inputs(306, Nq=5, Nk=3)
     with pytest.raises(ValueError):
         oracle_lib.attention_qk(q, k, v, 0.1, True)
+
+
+# --------------------------------------------------------------------------
+# the GEMM oracle (C = A B^T)
+
+
+def test_gemm_brute_force_triple_loop(oracle_lib):
+    g = torch.Generator().manual_seed(401)
+    a = torch.randn((5, 7), generator=g).to(torch.bfloat16)
+    b = torch.randn((3, 7), generator=g).to(torch.bfloat16)
+    c, mag = oracle_lib.gemm_abt(a, b)
+    A, B = widen(a), widen(b)
+    for i in range(5):
+        for j in range(3):
+            ref = 0.0
+            absref = 0.0
+            for k in range(7):
+                ref += A[i, k] * B[j, k]
+                absref += abs(A[i, k] * B[j, k])
+            assert abs(c[i, j] - ref) <= 1e-12
+            assert abs(mag[i, j] - absref) <= 1e-12
+
+
+def test_gemm_identity_and_transpose(oracle_lib):
+    # B = I returns A; swapping the operands transposes the product
+    g = torch.Generator().manual_seed(402)
+    a = torch.randn((6, 6), generator=g).to(torch.bfloat16)
+    b = torch.randn((4, 6), generator=g).to(torch.bfloat16)
+    eye = torch.eye(6).to(torch.bfloat16)
+    c, _ = oracle_lib.gemm_abt(a, eye)
+    np.testing.assert_array_equal(c, widen(a))
+    c1, _ = oracle_lib.gemm_abt(a, b)
+    c2, _ = oracle_lib.gemm_abt(b, a)
+    np.testing.assert_allclose(c1, c2.T, atol=1e-12)
+
+
+def test_gemm_golden_small(oracle_lib):
+    # hand-computed: rows of A against rows of B
+    a = bits([[1.0, 2.0, 0.5], [-1.0, 0.0, 4.0]])
+    b = bits([[2.0, -1.0, 8.0], [0.25, 0.5, -2.0]])
+    c, mag = oracle_lib.gemm_abt(a, b)
+    np.testing.assert_array_equal(c, [[2 - 2 + 4, 0.25 + 1 - 1], [-2 + 0 + 32, -0.25 + 0 - 8]])
+    np.testing.assert_array_equal(mag, [[2 + 2 + 4, 0.25 + 1 + 1], [2 + 0 + 32, 0.25 + 0 + 8]])
