@@ -4,13 +4,15 @@ O = softmax(scale * Q K^T [+ causal mask]) V with the per-row log-sum-exp, on
 bf16 [B, H, N, D] tensors, computed by hand-written sm_103a CUDA kernels behind
 a C ABI (``include/tk_attn.h``).  This package is the thin Python binding over
 that library: argument marshalling only.  The shared library is loaded on first
-use; if it is missing or cannot be loaded, every call raises.
+use; if it is missing or cannot be loaded, every call raises.  The library
+also holds a bf16 GEMM (C = A B^T) on the same TMA / tensor-core pipeline.
 """
 from .api import (  # noqa: F401
     TkAttnError,
     attention_forward,
     attention_forward_host,
     attention_forward_splitkv,
+    gemm_bf16,
     last_device_error,
     library,
     status_string,
@@ -21,5 +23,7 @@ from .api import (  # noqa: F401
     tk_attn_splitkv_workspace_bytes,
     tk_attn_status_string,
     tk_attn_version,
+    tk_gemm_bf16,
+    tk_gemm_bf16_check_args,
     version,
 )

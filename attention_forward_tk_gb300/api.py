@@ -39,6 +39,8 @@ EXPORTED = (
     "tk_attn_version",
     "tk_attn_last_device_error",
     "tk_attn_debug_drop_load",
+    "tk_gemm_bf16",
+    "tk_gemm_bf16_check_args",
 )
 
 
@@ -88,6 +90,10 @@ def library() -> ctypes.CDLL:
         lib.tk_attn_last_device_error.argtypes = [vp]
         lib.tk_attn_debug_drop_load.restype = None
         lib.tk_attn_debug_drop_load.argtypes = [i]
+        lib.tk_gemm_bf16.restype = i
+        lib.tk_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, vp]
+        lib.tk_gemm_bf16_check_args.restype = i
+        lib.tk_gemm_bf16_check_args.argtypes = [vp, vp, vp, i, i, i]
         _lib = lib
         return _lib
 
@@ -142,6 +148,14 @@ def tk_attn_last_device_error(stream: int) -> int:
 
 def tk_attn_debug_drop_load(enable: int) -> None:
     library().tk_attn_debug_drop_load(int(enable))
+
+
+def tk_gemm_bf16(a: int, b: int, c: int, M: int, N: int, K: int, stream: int) -> int:
+    return int(library().tk_gemm_bf16(a, b, c, M, N, K, stream))
+
+
+def tk_gemm_bf16_check_args(a: int, b: int, c: int, M: int, N: int, K: int) -> int:
+    return int(library().tk_gemm_bf16_check_args(a, b, c, M, N, K))
 
 
 # short aliases
@@ -228,6 +242,27 @@ def attention_forward_splitkv(q, k, v, scale: float | None = None, num_splits: i
                                lse.data_ptr(), B, H, Nq, Nk, D, float(scale), int(num_splits),
                                ws_ptr, ws_bytes, _stream_handle(stream)))
     return out, lse
+
+
+def gemm_bf16(a, b, out=None, stream=None):
+    """C = A B^T for bf16 CUDA tensors a [M, K] and b [N, K] (fp32 accumulation,
+    bf16 result [M, N]).  Enqueued on `stream`; returns immediately.
+    """
+    import torch
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError("a must be [M, K] and b [N, K]")
+    for t in (a, b):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("a, b must be contiguous bf16 CUDA tensors")
+    M, K = (int(x) for x in a.shape)
+    N = int(b.shape[0])
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    st = tk_gemm_bf16(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
+                      _stream_handle(stream))
+    if st != TK_ATTN_OK:
+        raise TkAttnError(f"tk_gemm_bf16: {tk_attn_status_string(st)} ({st})", st)
+    return out
 
 
 def attention_forward_host(q, k, v, causal: bool = False, scale: float | None = None,

@@ -1,6 +1,7 @@
 // tk_attn.cu -- host side of the attention forward library: argument checks,
 // TMA tensor-map encoding, persistent-grid sizing and the C ABI declared in
-// include/tk_attn.h.  The device work is in tk_attn_fwd.cuh.
+// include/tk_attn.h.  The device work is in tk_attn_fwd.cuh (attention),
+// tk_attn_combine.cuh (key-range merge) and tk_gemm.cuh (bf16 GEMM).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -18,6 +19,7 @@
 #include "tk_attn.h"
 #include "tk_attn_combine.cuh"
 #include "tk_attn_fwd.cuh"
+#include "tk_gemm.cuh"
 
 namespace tkattn {
 namespace {
@@ -85,6 +87,9 @@ void init_device(int dev, DeviceState &ds) {
   if (!st) st = configure_kernel<128, true>();
   if (!st) st = configure_kernel<64, false, true>();
   if (!st) st = configure_kernel<128, false, true>();
+  if (!st && cudaFuncSetAttribute(tk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  GemmCfg::kSmemAlloc) != cudaSuccess)
+    st = TK_ATTN_ERR_LAUNCH;
   if (!st && cudaGetSymbolAddress(reinterpret_cast<void **>(&ds.err_word), g_dev_error) !=
                  cudaSuccess)
     st = TK_ATTN_ERR_LAUNCH;
@@ -131,6 +136,22 @@ bool make_map(CUtensorMap *map, const void *ptr, int BH, int N, int D) {
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows, K] bf16 row-major as a 2-D tensor (k fastest); boxes of 64 columns
+// x box_rows rows, 128-byte swizzle.  Rows past `rows` and columns past K
+// read as zero, so ragged tiles add nothing to the sums.
+bool make_map_2d(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -451,6 +472,57 @@ extern "C" int tk_attn_fwd_splitkv_static(const void *q, const void *k, const vo
   if (split_workspace(BH, Nq, D, S) > kStaticScratchBytes) return TK_ATTN_ERR_TOO_LARGE;
   return tk_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, D, scale, num_splits,
                              ds->static_scratch, kStaticScratchBytes, stream);
+}
+
+// ---------------------------------------------------------------- GEMM
+
+extern "C" int tk_gemm_bf16_check_args(const void *a, const void *b, const void *c, int M,
+                                       int N, int K) {
+  if (!a || !b || !c) return TK_ATTN_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return TK_ATTN_ERR_INVALID_ARG;
+  if (((uintptr_t)a | (uintptr_t)b | (uintptr_t)c) & 15u) return TK_ATTN_ERR_UNSUPPORTED;
+  // row strides of A, B (K * 2 bytes) and C (N * 2 bytes) must be 16-byte multiples
+  if ((K & 7) || (N & 7)) return TK_ATTN_ERR_UNSUPPORTED;
+  const unsigned long long abytes = (unsigned long long)M * K * 2ull;
+  const unsigned long long bbytes = (unsigned long long)N * K * 2ull;
+  const unsigned long long cbytes = (unsigned long long)M * N * 2ull;
+  if (abytes >= (1ull << 40) || bbytes >= (1ull << 40)) return TK_ATTN_ERR_UNSUPPORTED;
+  const long long tiles = ((M + (long long)GemmCfg::kBM - 1) / GemmCfg::kBM) *
+                          ((N + (long long)GemmCfg::kBN - 1) / GemmCfg::kBN);
+  if (tiles > 0x7fffffffLL) return TK_ATTN_ERR_UNSUPPORTED;
+  if (overlaps((uintptr_t)c, cbytes, (uintptr_t)a, abytes) ||
+      overlaps((uintptr_t)c, cbytes, (uintptr_t)b, bbytes))
+    return TK_ATTN_ERR_INVALID_ARG;
+  return TK_ATTN_OK;
+}
+
+extern "C" int tk_gemm_bf16(const void *a, const void *b, void *c, int M, int N, int K,
+                            tk_attn_stream_t stream) {
+  int st = tk_gemm_bf16_check_args(a, b, c, M, N, K);
+  if (st) return st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0 || N == 0) return TK_ATTN_OK;  // an empty C: nothing to write
+  if (K == 0)                               // empty sums: C = 0
+    return cudaMemsetAsync(c, 0, (size_t)M * N * 2, s) == cudaSuccess ? TK_ATTN_OK
+                                                                     : TK_ATTN_ERR_LAUNCH;
+  CUtensorMap ta, tb;
+  if (!make_map_2d(&ta, a, M, K, GemmCfg::kBM) || !make_map_2d(&tb, b, N, K, GemmCfg::kBN))
+    return TK_ATTN_ERR_LAUNCH;
+  GemmParams p;
+  p.c = static_cast<__nv_bfloat16 *>(c);
+  p.err = ds->err_word;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_m = (M + GemmCfg::kBM - 1) / GemmCfg::kBM;
+  p.tiles_n = (N + GemmCfg::kBN - 1) / GemmCfg::kBN;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.k_blocks = (K + GemmCfg::kBK - 1) / GemmCfg::kBK;
+  const int grid = p.num_tiles < ds->num_sms ? p.num_tiles : ds->num_sms;
+  tk_gemm_kernel<<<grid, GemmCfg::kThreads, GemmCfg::kSmemAlloc, s>>>(ta, tb, p);
+  return cudaGetLastError() == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 
 extern "C" const char *tk_attn_status_string(int status) {

@@ -19,6 +19,10 @@ them, split over keys):
 
   prefill_q256_k32k_d128  B 1, H 32, Nq 256, Nk 32768, D 128, unmasked, N(0, 1)
 
+and one dense GEMM shape for tk_gemm_bf16 (C = A B^T):
+
+  gemm_8192   M = N = K = 8192, A and B ~ N(0, 1)
+
 The scale is 1/sqrt(D) in every workload (the kernel examples on the pages use
 1/sqrt(64) = 0.125 and 1/sqrt(128) ~= 0.08838834764).
 
@@ -129,6 +133,40 @@ def draw(shape, seed: int, dist: str = "normal", device="cpu", kv_shape=None):
     else:
         raise ValueError(f"unknown distribution {dist!r}")
     return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
+
+
+@dataclass(frozen=True)
+class GemmWorkload:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def io_bytes(self) -> int:
+        """A and B read, C written, bf16."""
+        return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
+
+
+# The square bf16 product the pages compare with cuBLAS, at the size the
+# cuBLAS peak of this GPU is measured on.
+GEMM_WORKLOADS = (GemmWorkload("gemm_8192", 8192, 8192, 8192, 6),)
+GEMM_BY_NAME = {w.name: w for w in GEMM_WORKLOADS}
+
+
+def draw_gemm(M: int, N: int, K: int, seed: int, device="cpu"):
+    """A [M, K] then B [N, K], N(0, 1) rounded to bf16, from one generator
+    seeded with `seed` (the same recipe as draw())."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    a = _randn(g, (M, K))
+    b = _randn(g, (N, K))
+    return a.to(torch.bfloat16), b.to(torch.bfloat16)
 
 
 def workload_inputs(w: Workload, device="cpu"):

@@ -3,6 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tk|reference]
                     [--workload NAME] [--all-workloads]
 
+`--workload gemm_8192` times the library's bf16 GEMM (tk_gemm_bf16, C = A B^T,
+M = N = K = 8192) instead, with cuBLAS (torch.matmul) on the same operands
+beside it.
+
 One step = one tk_attn_fwd call (the whole hot path: TMA loads, QK^T,
 online softmax, PV, epilogue) over one batch of synthetic inputs resident in
 HBM.  The default workload is B16 H16 N1024 D64 non-causal; the metric is
@@ -254,6 +258,50 @@ def time_gpu(w, steps: int, warmup: int, device):
     return ms, wall, steps * per_call
 
 
+def time_gemm(gw, steps: int, warmup: int, device, cublas: bool = True):
+    """CUDA-event times of `steps` tk_gemm_bf16 launches on one pair of
+    operands (L2 flushed before each), and of torch.matmul (cuBLAS) on the
+    same operands beside it."""
+    import torch
+
+    from attention_forward_tk_gb300 import api
+    from attention_forward_tk_gb300.inputs import draw_gemm
+
+    a, b = draw_gemm(gw.M, gw.N, gw.K, gw.seed, device=device)
+    c = torch.empty((gw.M, gw.N), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+
+    def ours():
+        st = api.tk_gemm_bf16(a.data_ptr(), b.data_ptr(), c.data_ptr(), gw.M, gw.N, gw.K, sh)
+        if st:
+            raise RuntimeError(api.tk_attn_status_string(st))
+
+    def theirs():
+        torch.matmul(a, b.t(), out=c)
+
+    def run(fn):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        torch.cuda.synchronize(device)
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize(device)
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    ms = run(ours)
+    if api.tk_attn_last_device_error(sh) != 0:
+        raise RuntimeError("device-side barrier timeout in tk_gemm_bf16")
+    return ms, (run(theirs) if cublas else None)
+
+
 def time_e2e(w, steps: int, warmup: int, device):
     """The same call from pinned host buffers: H2D of Q, K, V, the kernel, and
     D2H of O and LSE every step, timed with CUDA events around all of it."""
@@ -318,15 +366,20 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="budget of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true",
+                    help="GEMM workload: skip the cuBLAS comparison (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer leg (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from attention_forward_tk_gb300.inputs import BY_NAME, EXTRA_WORKLOADS, WORKLOADS
-    w = BY_NAME[args.workload]
+    from attention_forward_tk_gb300.inputs import (BY_NAME, EXTRA_WORKLOADS, GEMM_BY_NAME,
+                                                   GEMM_WORKLOADS, WORKLOADS)
     world, rank, local = dist_env()
+    if args.workload in GEMM_BY_NAME:
+        return main_gemm(args, GEMM_BY_NAME[args.workload], world, rank, local)
+    w = BY_NAME[args.workload]
 
     if args.impl == "reference":
         return main_reference(args, w, world, rank)
@@ -381,6 +434,15 @@ def main():
             c = oclk.summary()
             extra[ow.name] = {"ms": round(m, 4), "tflops": round(ow.flops / m / 1e9, 1),
                               "launches": n, "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
+        for gw in GEMM_WORKLOADS:
+            with ClockSampler(device.index if world == 1 else local) as oclk:
+                gms, cms = time_gemm(gw, 100, 5, device)
+            m, mc = statistics.median(gms), statistics.median(cms)
+            c = oclk.summary()
+            extra[gw.name] = {"ms": round(m, 4), "tflops": round(gw.flops / m / 1e9, 1),
+                              "launches": 100, "cublas_ms": round(mc, 4),
+                              "cublas_tflops": round(gw.flops / mc / 1e9, 1),
+                              "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
 
     if rank != 0:
         if world > 1:
@@ -446,6 +508,45 @@ def main():
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def main_gemm(args, gw, world, rank, local):
+    """`--workload gemm_8192`: the bf16 GEMM of the library (tk_gemm_bf16)
+    timed alone, cuBLAS (torch.matmul) on the same operands beside it."""
+    import torch
+
+    from attention_forward_tk_gb300.build import build_library
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    build_library()
+    with ClockSampler(device.index) as clk:
+        ms, cms = time_gemm(gw, args.steps, args.warmup, device,
+                            cublas=not args.no_cublas)
+    if rank != 0:
+        return
+    peak_tf, _, peak_kind = measured_peaks()
+    kernel_ms = statistics.mean(ms)
+    achieved = gw.flops / (kernel_ms / 1e3) / 1e12
+    line = {
+        "metric": "bf16 GEMM C = A B^T TFLOP/s (1xGB300)",
+        "value": round(achieved, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(kernel_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": gw.name, "M": gw.M, "N": gw.N, "K": gw.K,
+                   "flops_per_step": gw.flops,
+                   "l2": "flushed (256 MB write) before every timed step"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                     "peak_kind": f"{peak_kind} dense bf16 (burst)", "traffic": None,
+                     "algorithmic_bytes": gw.io_bytes},
+        "cublas": None if cms is None else {
+            "ms": round(statistics.mean(cms), 5),
+            "tflops": round(gw.flops / (statistics.mean(cms) / 1e3) / 1e12, 1)},
+        "gpu_launches": args.steps,
+        "kernel_ms_median": round(statistics.median(ms), 5),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
 
 
 def main_reference(args, w, world, rank):

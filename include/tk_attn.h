@@ -61,7 +61,7 @@ typedef struct CUstream_st *tk_attn_stream_t;
 #define TK_ATTN_ERR_TOO_LARGE (-6)      /* tk_attn_fwd_splitkv_static: the ranges'
                                            partial results exceed its static scratch */
 
-#define TK_ATTN_VERSION 10100 /* major*10000 + minor*100 + patch */
+#define TK_ATTN_VERSION 10200 /* major*10000 + minor*100 + patch */
 
 /*
  * tk_attn_fwd -- fused attention forward, asynchronous on `stream`.
@@ -162,6 +162,33 @@ size_t tk_attn_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int D, int 
 int tk_attn_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o,
                                float *lse, int B, int H, int Nq, int Nk, int D, float scale,
                                int num_splits, tk_attn_stream_t stream);
+
+/*
+ * tk_gemm_bf16 -- dense bf16 matrix product with fp32 accumulation:
+ *
+ *   C[i, j] = sum_k A[i, k] * B[j, k]      (C = A B^T), rounded once to bf16
+ *
+ * The ThunderKittens paper summary ("ThunderKittens: Simple, Fast, and
+ * Adorable AI Kernels", shd-paper.top, abstract and results) reports GEMM
+ * at cuBLAS speed as one of the library's kernels; the operation is the
+ * textbook product, written here in the layout its tiles use (both operands
+ * K-major, as a linear layer's weight is stored).
+ *
+ *   a : bf16 [M, K] row-major      b : bf16 [N, K] row-major
+ *   c : bf16 [M, N] row-major      (device memory owned by the caller)
+ *
+ * M, N, K >= 0.  N and K must be multiples of 8 (16-byte row strides) and
+ * the three base addresses 16-byte aligned, else TK_ATTN_ERR_UNSUPPORTED.
+ * M == 0 or N == 0 enqueues nothing; K == 0 sets C to zero.  c must not
+ * overlap a or b (TK_ATTN_ERR_INVALID_ARG).  Same stream, allocation and
+ * error conventions as tk_attn_fwd; a barrier wait that runs out is reported
+ * by tk_attn_last_device_error.
+ */
+int tk_gemm_bf16(const void *a, const void *b, void *c, int M, int N, int K,
+                 tk_attn_stream_t stream);
+
+/* The argument checks of tk_gemm_bf16 alone (no GPU needed). */
+int tk_gemm_bf16_check_args(const void *a, const void *b, const void *c, int M, int N, int K);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char *tk_attn_status_string(int status);

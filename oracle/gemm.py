@@ -6,10 +6,10 @@ library matrix product (numpy, float64) serves as the one step, as a plain
 definition allows.  Also returns the per-element magnitude sum
 sum_k |a_ik b_jk|, which bounds the rounding of any fp32 accumulation order.
 
-Source: the GEMM the ThunderKittens pages benchmark against cuBLAS (the
-"matches cuBLAS" claim of the ThunderKittens news write-up, 88811315.cn,
-post 77732); the pages give no kernel for it, only that the tile primitives
-reach cuBLAS speed, so the definition here is the textbook one.
+Source: the GEMM the ThunderKittens paper summary benchmarks against cuBLAS
+("ThunderKittens: Simple, Fast, and Adorable AI Kernels", shd-paper.top,
+abstract and experimental highlights: GEMM on a par with cuBLAS); the pages
+give no kernel for it, so the definition here is the textbook one.
 """
 import numpy as np
 

@@ -14,7 +14,7 @@ HEADER = os.path.join(ROOT, "include", "tk_attn.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tk_attn_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(tk_(?:attn|gemm)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_names(tk_lib):
@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol(tk_lib):
 
 
 def test_version_and_status_strings(tk_lib):
-    assert tk_lib.tk_attn_version() == 10100
+    assert tk_lib.tk_attn_version() == 10200
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = tk_lib.tk_attn_status_string(code)
         assert s and s != "unknown status"
@@ -119,3 +119,25 @@ def test_splitkv_workspace_query_without_a_gpu(tk_lib):
         pytest.skip("a GPU is present")
     assert tk_lib.tk_attn_splitkv_workspace_bytes(1, 2, 16, 300, 64, 4) == 0
     assert tk_lib.tk_attn_splitkv_workspace_bytes(1, 2, 16, 300, 96, 4) == 0
+
+
+def test_gemm_rejects_bad_arguments_before_touching_cuda(tk_lib):
+    A, B_, C = Q, K, O
+
+    def chk(a=A, b=B_, c=C, M=256, N=512, K=128):
+        return tk_lib.tk_gemm_bf16_check_args(a, b, c, M, N, K)
+    assert chk() == tk_lib.TK_ATTN_OK
+    assert chk(M=0) == tk_lib.TK_ATTN_OK and chk(K=0) == tk_lib.TK_ATTN_OK
+    assert chk(a=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(M=-1) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(K=-8) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(N=500) == tk_lib.TK_ATTN_ERR_UNSUPPORTED   # row stride of C not 16 bytes
+    assert chk(K=100) == tk_lib.TK_ATTN_ERR_UNSUPPORTED   # row stride of A, B not 16 bytes
+    assert chk(b=B_ + 8) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    # C [256, 512] bf16 = 256 KiB starting inside A (64 KiB) or B (128 KiB)
+    assert chk(c=A + 4096) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(c=B_ - 4096) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    # A and B may alias (C = A A^T)
+    assert chk(b=A, N=256) == tk_lib.TK_ATTN_OK
+    # the full call checks first, so it needs no GPU to reject
+    assert tk_lib.tk_gemm_bf16(A, B_, C, 256, 500, 128, 0) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
