@@ -47,6 +47,7 @@ struct DeviceState {
   int num_sms = 0;
   int *err_word = nullptr;  // address of g_dev_error on this device
   void *static_scratch = nullptr;  // address of g_splitkv_scratch on this device
+  int gemm_pairs = 0;  // CTA pairs of tk_gemm_kernel that fit on the device at once
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -90,6 +91,21 @@ void init_device(int dev, DeviceState &ds) {
   if (!st && cudaFuncSetAttribute(tk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   GemmCfg::kSmemAlloc) != cudaSuccess)
     st = TK_ATTN_ERR_LAUNCH;
+  if (!st) {
+    // Pairs live on the two SMs of a TPC; ask how many fit at once rather
+    // than assume every SM has a partner.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ds.num_sms, 1, 1);
+    cfg.blockDim = dim3(GemmCfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = GemmCfg::kSmemAlloc;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, tk_gemm_kernel, &cfg) != cudaSuccess ||
+        clusters <= 0) {
+      cudaGetLastError();
+      clusters = ds.num_sms / 2;
+    }
+    ds.gemm_pairs = clusters;
+  }
   if (!st && cudaGetSymbolAddress(reinterpret_cast<void **>(&ds.err_word), g_dev_error) !=
                  cudaSuccess)
     st = TK_ATTN_ERR_LAUNCH;
@@ -508,7 +524,7 @@ extern "C" int tk_gemm_bf16(const void *a, const void *b, void *c, int M, int N,
     return cudaMemsetAsync(c, 0, (size_t)M * N * 2, s) == cudaSuccess ? TK_ATTN_OK
                                                                      : TK_ATTN_ERR_LAUNCH;
   CUtensorMap ta, tb;
-  if (!make_map_2d(&ta, a, M, K, GemmCfg::kBM) || !make_map_2d(&tb, b, N, K, GemmCfg::kBN))
+  if (!make_map_2d(&ta, a, M, K, GemmCfg::kHalf) || !make_map_2d(&tb, b, N, K, GemmCfg::kHalf))
     return TK_ATTN_ERR_LAUNCH;
   GemmParams p;
   p.c = static_cast<__nv_bfloat16 *>(c);
@@ -520,8 +536,8 @@ extern "C" int tk_gemm_bf16(const void *a, const void *b, void *c, int M, int N,
   p.tiles_n = (N + GemmCfg::kBN - 1) / GemmCfg::kBN;
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.k_blocks = (K + GemmCfg::kBK - 1) / GemmCfg::kBK;
-  const int grid = p.num_tiles < ds->num_sms ? p.num_tiles : ds->num_sms;
-  tk_gemm_kernel<<<grid, GemmCfg::kThreads, GemmCfg::kSmemAlloc, s>>>(ta, tb, p);
+  const int pairs = p.num_tiles < ds->gemm_pairs ? p.num_tiles : ds->gemm_pairs;
+  tk_gemm_kernel<<<2 * pairs, GemmCfg::kThreads, GemmCfg::kSmemAlloc, s>>>(ta, tb, p);
   return cudaGetLastError() == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 
