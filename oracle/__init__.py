@@ -12,6 +12,8 @@ Contents
   attention_qk_rows, attention_qk
                    the same definition for Nq queries against Nk keys
                    (inference shape); causal aligned to the last key
+  attention_bwd    dQ, dK, dV of the same definition for a given dO (numpy,
+                   fp64), with the magnitude sums that bound kernel rounding
   gemm_abt         C = A B^T for bf16 A [M, K], B [N, K] in float64, with the
                    per-element magnitude sum that bounds fp32 accumulation
   tiled_online_softmax
@@ -29,10 +31,12 @@ log over scaled, masked scores).
 """
 from .brute import (attention, attention_qk, attention_qk_rows, attention_rows, build, lib_path,
                     max_threads)
+from .backward import attention_bwd
 from .gemm import gemm_abt
 from .tiled import tiled_online_softmax
 
 __all__ = [
+    "attention_bwd",
     "attention",
     "attention_qk",
     "attention_qk_rows",

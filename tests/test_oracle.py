@@ -365,3 +365,104 @@ def test_gemm_golden_small(oracle_lib):
     c, mag = oracle_lib.gemm_abt(a, b)
     np.testing.assert_array_equal(c, [[2 - 2 + 4, 0.25 + 1 - 1], [-2 + 0 + 32, -0.25 + 0 - 8]])
     np.testing.assert_array_equal(mag, [[2 + 2 + 4, 0.25 + 1 + 1], [2 + 0 + 32, 0.25 + 0 + 8]])
+
+
+# --------------------------------------------------------------------------
+# the backward oracle (dQ, dK, dV)
+
+
+def _fwd_loss64(Q, K, V, dO, scale, causal):
+    """sum(dO * O) with O from float64 torch.softmax: an independent forward."""
+    s = scale * (Q @ K.transpose(-1, -2))
+    if causal:
+        n = Q.shape[-2]
+        s = s.masked_fill(~torch.ones(n, n, dtype=torch.bool).tril(), float("-inf"))
+    return (dO * (torch.softmax(s, dim=-1) @ V)).sum()
+
+
+def _bwd_inputs(seed, shape, dist=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return tuple((dist * torch.randn(shape, generator=g)).to(torch.bfloat16) for _ in range(4))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_matches_float64_autograd(oracle_lib, causal):
+    q, k, v, do = _bwd_inputs(501 + causal, (2, 2, 37, 16))
+    r = oracle_lib.attention_bwd(q, k, v, do, 0.3, causal)
+    Q, K, V = (t.double().requires_grad_() for t in (q, k, v))
+    _fwd_loss64(Q, K, V, do.double(), 0.3, causal).backward()
+    for name, t in (("dq", Q), ("dk", K), ("dv", V)):
+        np.testing.assert_allclose(r[name], t.grad.numpy().reshape(4, 37, 16), rtol=1e-10,
+                                   atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_matches_finite_differences(oracle_lib, causal):
+    # central differences of sum(dO * O) at the bf16 point, in float64
+    q, k, v, do = _bwd_inputs(511 + causal, (1, 1, 9, 4), dist=1.5)
+    r = oracle_lib.attention_bwd(q, k, v, do, 0.7, causal)
+    base = [t.double() for t in (q, k, v)]
+    dO = do.double()
+    h = 1e-6
+    rng = np.random.default_rng(3)
+    for which, name in enumerate(("dq", "dk", "dv")):
+        for _ in range(6):
+            i, d = int(rng.integers(9)), int(rng.integers(4))
+            plus = [t.clone() for t in base]
+            minus = [t.clone() for t in base]
+            plus[which][0, 0, i, d] += h
+            minus[which][0, 0, i, d] -= h
+            fd = (_fwd_loss64(*plus, dO, 0.7, causal) - _fwd_loss64(*minus, dO, 0.7, causal)) / (2 * h)
+            assert abs(float(fd) - r[name][0, i, d]) <= 1e-7 * (1 + abs(float(fd))), (name, i, d)
+
+
+def test_bwd_single_key(oracle_lib):
+    # one key: P = 1, so dV = dO and the softmax passes no gradient to S
+    q, k, v, do = _bwd_inputs(521, (1, 2, 1, 8))
+    r = oracle_lib.attention_bwd(q, k, v, do, 0.5, False)
+    np.testing.assert_array_equal(r["dv"], widen(do).reshape(2, 1, 8))
+    assert np.abs(r["dq"]).max() <= 1e-15 and np.abs(r["dk"]).max() <= 1e-15
+
+
+def test_bwd_causal_first_row_and_last_key(oracle_lib):
+    # causal: query 0 sees key 0 only (dQ_0 = 0); key N-1 is seen by query
+    # N-1 only, so dV_{N-1} = P_{N-1,N-1} dO_{N-1}
+    q, k, v, do = _bwd_inputs(531, (1, 1, 12, 8))
+    r = oracle_lib.attention_bwd(q, k, v, do, 0.4, True)
+    assert np.abs(r["dq"][0, 0]).max() <= 1e-15
+    Q, K = widen(q)[0, 0], widen(k)[0, 0]
+    s = 0.4 * Q[11] @ K.T
+    p_last = math.exp(s[11] - s.max()) / np.exp(s - s.max()).sum()
+    np.testing.assert_allclose(r["dv"][0, 11], p_last * widen(do)[0, 0, 11], rtol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_dk_sums_to_zero_over_keys(oracle_lib, causal):
+    # every row of dS sums to zero (a softmax row is shift-invariant), so
+    # sum_j dK_j = scale sum_i (sum_j dS_ij) q_i = 0
+    q, k, v, do = _bwd_inputs(541 + causal, (1, 2, 40, 8))
+    r = oracle_lib.attention_bwd(q, k, v, do, 0.25, causal)
+    assert np.abs(r["dk"].sum(axis=1)).max() <= 1e-12 * (1 + np.abs(r["dk"]).max())
+
+
+def test_bwd_key_shift_leaves_dq_and_dv(oracle_lib):
+    # adding one vector c to every key shifts each score row by q_i . c,
+    # which the softmax ignores: P, dS, dV and dQ are unchanged (dK moves)
+    g = torch.Generator().manual_seed(551)
+    ints = lambda shape: (torch.randint(-8, 9, shape, generator=g).float() / 8)
+    q, k, v, do = (ints((1, 1, 10, 4)) for _ in range(4))
+    c = ints((4,))
+    r0 = oracle_lib.attention_bwd(*(bits(t.numpy()) for t in (q, k, v, do)), 0.5, False)
+    r1 = oracle_lib.attention_bwd(*(bits(t.numpy()) for t in (q, k + c, v, do)), 0.5, False)
+    np.testing.assert_allclose(r1["dq"], r0["dq"], atol=1e-12)
+    np.testing.assert_allclose(r1["dv"], r0["dv"], atol=1e-12)
+
+
+def test_bwd_slices_and_magnitudes(oracle_lib):
+    q, k, v, do = _bwd_inputs(561, (2, 3, 20, 8))
+    full = oracle_lib.attention_bwd(q, k, v, do, 0.3, True)
+    part = oracle_lib.attention_bwd(q, k, v, do, 0.3, True, slices=[4, 1])
+    for name in full:
+        np.testing.assert_array_equal(part[name], full[name][[4, 1]])
+    for g in ("dq", "dk", "dv"):
+        assert (full["mag_" + g] >= np.abs(full[g]) - 1e-12).all()
