@@ -5,10 +5,12 @@ bf16 [B, H, N, D] tensors, computed by hand-written sm_103a CUDA kernels behind
 a C ABI (``include/tk_attn.h``).  This package is the thin Python binding over
 that library: argument marshalling only.  The shared library is loaded on first
 use; if it is missing or cannot be loaded, every call raises.  The library
-also holds a bf16 GEMM (C = A B^T) on the same TMA / tensor-core pipeline.
+also holds the backward pass (dQ, dK, dV) and a bf16 GEMM (C = A B^T) on the
+same TMA / tensor-core pipeline.
 """
 from .api import (  # noqa: F401
     TkAttnError,
+    attention_backward,
     attention_forward,
     attention_forward_host,
     attention_forward_splitkv,
@@ -16,6 +18,9 @@ from .api import (  # noqa: F401
     last_device_error,
     library,
     status_string,
+    tk_attn_bwd,
+    tk_attn_bwd_check_args,
+    tk_attn_bwd_workspace_bytes,
     tk_attn_check_args,
     tk_attn_fwd,
     tk_attn_fwd_splitkv,

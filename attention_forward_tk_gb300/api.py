@@ -41,6 +41,9 @@ EXPORTED = (
     "tk_attn_debug_drop_load",
     "tk_gemm_bf16",
     "tk_gemm_bf16_check_args",
+    "tk_attn_bwd",
+    "tk_attn_bwd_workspace_bytes",
+    "tk_attn_bwd_check_args",
 )
 
 
@@ -90,6 +93,14 @@ def library() -> ctypes.CDLL:
         lib.tk_attn_last_device_error.argtypes = [vp]
         lib.tk_attn_debug_drop_load.restype = None
         lib.tk_attn_debug_drop_load.argtypes = [i]
+        lib.tk_attn_bwd.restype = i
+        lib.tk_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp,
+                                    ctypes.c_size_t, vp]
+        lib.tk_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.tk_attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        lib.tk_attn_bwd_check_args.restype = i
+        lib.tk_attn_bwd_check_args.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
+                                               vp, ctypes.c_size_t]
         lib.tk_gemm_bf16.restype = i
         lib.tk_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, vp]
         lib.tk_gemm_bf16_check_args.restype = i
@@ -148,6 +159,26 @@ def tk_attn_last_device_error(stream: int) -> int:
 
 def tk_attn_debug_drop_load(enable: int) -> None:
     library().tk_attn_debug_drop_load(int(enable))
+
+
+def tk_attn_bwd(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, dk: int,
+                dv: int, B: int, H: int, N: int, D: int, scale: float, causal: int,
+                workspace: int, workspace_bytes: int, stream: int) -> int:
+    return int(library().tk_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D,
+                                     ctypes.c_float(scale), int(causal), workspace,
+                                     int(workspace_bytes), stream))
+
+
+def tk_attn_bwd_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return int(library().tk_attn_bwd_workspace_bytes(B, H, N, D))
+
+
+def tk_attn_bwd_check_args(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int,
+                           dk: int, dv: int, B: int, H: int, N: int, D: int, scale: float,
+                           workspace: int, workspace_bytes: int) -> int:
+    return int(library().tk_attn_bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D,
+                                                 ctypes.c_float(scale), workspace,
+                                                 int(workspace_bytes)))
 
 
 def tk_gemm_bf16(a: int, b: int, c: int, M: int, N: int, K: int, stream: int) -> int:
@@ -242,6 +273,37 @@ def attention_forward_splitkv(q, k, v, scale: float | None = None, num_splits: i
                                lse.data_ptr(), B, H, Nq, Nk, D, float(scale), int(num_splits),
                                ws_ptr, ws_bytes, _stream_handle(stream)))
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+                       dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV for bf16 CUDA tensors [B, H, N, D], given the forward's o and
+    lse (from attention_forward on the same inputs) and the output gradient
+    dout.  Enqueued on `stream`; returns immediately.  Outputs and the
+    workspace are allocated by torch when not given.
+    """
+    import torch
+    if q.dim() != 4 or any(t.shape != q.shape for t in (k, v, o, dout)):
+        raise ValueError("q, k, v, o, dout must be [B, H, N, D] tensors of one shape")
+    B, H, N, D = (int(x) for x in q.shape)
+    for t in (q, k, v, o, dout):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = tk_attn_bwd_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = tk_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
+                     float(scale), int(bool(causal)), workspace.data_ptr(),
+                     workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != TK_ATTN_OK:
+        raise TkAttnError(f"tk_attn_bwd: {tk_attn_status_string(st)} ({st})", st)
+    return dq, dk, dv
 
 
 def gemm_bf16(a, b, out=None, stream=None):

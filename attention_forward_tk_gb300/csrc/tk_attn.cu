@@ -18,6 +18,7 @@
 
 #include "tk_attn.h"
 #include "tk_attn_combine.cuh"
+#include "tk_attn_bwd.cuh"
 #include "tk_attn_fwd.cuh"
 #include "tk_gemm.cuh"
 
@@ -69,6 +70,18 @@ int configure_kernel() {
   return TK_ATTN_OK;
 }
 
+template <int D, bool kCausal>
+int configure_bwd() {
+  if (cudaFuncSetAttribute(tk_attn_bwd_dkdv_kernel<D, kCausal>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<D>::kSmemAlloc) != cudaSuccess ||
+      cudaFuncSetAttribute(tk_attn_bwd_dq_kernel<D, kCausal>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<D>::kSmemAlloc) != cudaSuccess)
+    return TK_ATTN_ERR_LAUNCH;
+  return TK_ATTN_OK;
+}
+
 // Per-device set-up, once, with that device current.
 void init_device(int dev, DeviceState &ds) {
   int major = 0, minor = 0;
@@ -88,6 +101,10 @@ void init_device(int dev, DeviceState &ds) {
   if (!st) st = configure_kernel<128, true>();
   if (!st) st = configure_kernel<64, false, true>();
   if (!st) st = configure_kernel<128, false, true>();
+  if (!st) st = configure_bwd<64, false>();
+  if (!st) st = configure_bwd<64, true>();
+  if (!st) st = configure_bwd<128, false>();
+  if (!st) st = configure_bwd<128, true>();
   if (!st && cudaFuncSetAttribute(tk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   GemmCfg::kSmemAlloc) != cudaSuccess)
     st = TK_ATTN_ERR_LAUNCH;
@@ -488,6 +505,126 @@ extern "C" int tk_attn_fwd_splitkv_static(const void *q, const void *k, const vo
   if (split_workspace(BH, Nq, D, S) > kStaticScratchBytes) return TK_ATTN_ERR_TOO_LARGE;
   return tk_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, D, scale, num_splits,
                              ds->static_scratch, kStaticScratchBytes, stream);
+}
+
+// ---------------------------------------------------------------- backward
+
+namespace tkattn {
+namespace {
+
+size_t bwd_workspace(long long BH, int N) {
+  const long long npad = (N + 127LL) / 128 * 128;
+  return (size_t)(2 * BH * npad) * sizeof(float);
+}
+
+template <int D, bool kCausal>
+cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, BwdParams p, const void *o, const void *dout,
+                       const float *lse, float *lse2, float *delta, int num_sms,
+                       cudaStream_t s) {
+  const long long rows = (long long)p.BH * p.Npad;
+  tk_attn_bwd_prep_kernel<D><<<(unsigned)((rows + kPrepWarps - 1) / kPrepWarps),
+                               kPrepWarps * 32, 0, s>>>(
+      static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dout), lse,
+      lse2, delta, p.N, p.Npad, rows);
+  p.num_units = p.BH * p.nt;
+  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+  tk_attn_bwd_dkdv_kernel<D, kCausal>
+      <<<grid, BwdCfg<D>::kThreads, BwdCfg<D>::kSmemAlloc, s>>>(tq, tk, tv, tdo, p);
+  tk_attn_bwd_dq_kernel<D, kCausal>
+      <<<grid, BwdCfg<D>::kThreads, BwdCfg<D>::kSmemAlloc, s>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace tkattn
+
+extern "C" size_t tk_attn_bwd_workspace_bytes(int B, int H, int N, int D) {
+  if (B <= 0 || H <= 0 || N <= 0 || (D != 64 && D != 128)) return 0;
+  return bwd_workspace((long long)B * H, N);
+}
+
+extern "C" int tk_attn_bwd_check_args(const void *q, const void *k, const void *v,
+                                      const void *o, const float *lse, const void *dout,
+                                      const void *dq, const void *dk, const void *dv, int B,
+                                      int H, int N, int D, float scale, const void *workspace,
+                                      size_t workspace_bytes) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return TK_ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return TK_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return TK_ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return TK_ATTN_ERR_UNSUPPORTED;
+  const uintptr_t ptrs[10] = {(uintptr_t)q,  (uintptr_t)k,  (uintptr_t)v,  (uintptr_t)o,
+                              (uintptr_t)lse, (uintptr_t)dout, (uintptr_t)dq, (uintptr_t)dk,
+                              (uintptr_t)dv, (uintptr_t)workspace};
+  uintptr_t any = 0;
+  for (uintptr_t x : ptrs) any |= x;
+  if (any & 15u) return TK_ATTN_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL || BH * ((N + 127LL) / 128) > 0x7fffffffLL) return TK_ATTN_ERR_UNSUPPORTED;
+  const unsigned long long tb = (unsigned long long)BH * N * D * 2ull;
+  if (tb >= (1ull << 40)) return TK_ATTN_ERR_UNSUPPORTED;
+  const size_t need = bwd_workspace(BH, N);
+  if (workspace_bytes < need) return TK_ATTN_ERR_INVALID_ARG;
+  // the outputs and the workspace overlap nothing else
+  const size_t lb = (size_t)BH * N * 4;
+  const uintptr_t outs[4] = {(uintptr_t)dq, (uintptr_t)dk, (uintptr_t)dv, (uintptr_t)workspace};
+  const size_t out_n[4] = {tb, tb, tb, need};
+  const uintptr_t ins[6] = {(uintptr_t)q, (uintptr_t)k, (uintptr_t)v, (uintptr_t)o,
+                            (uintptr_t)lse, (uintptr_t)dout};
+  const size_t in_n[6] = {tb, tb, tb, tb, lb, tb};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], out_n[a], ins[b], in_n[b])) return TK_ATTN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], out_n[a], outs[b], out_n[b])) return TK_ATTN_ERR_INVALID_ARG;
+  }
+  return TK_ATTN_OK;
+}
+
+extern "C" int tk_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                           int B, int H, int N, int D, float scale, int causal, void *workspace,
+                           size_t workspace_bytes, tk_attn_stream_t stream) {
+  int st = tk_attn_bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D, scale,
+                                  workspace, workspace_bytes);
+  if (st) return st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, BH, N, D) || !make_map(&tk, k, BH, N, D) ||
+      !make_map(&tv, v, BH, N, D) || !make_map(&tdo, dout, BH, N, D))
+    return TK_ATTN_ERR_LAUNCH;
+  BwdParams p;
+  p.dq = static_cast<__nv_bfloat16 *>(dq);
+  p.dk = static_cast<__nv_bfloat16 *>(dk);
+  p.dv = static_cast<__nv_bfloat16 *>(dv);
+  p.nt = (N + 127) / 128;
+  p.Npad = p.nt * 128;
+  float *lse2 = static_cast<float *>(workspace);
+  float *delta = lse2 + (size_t)BH * p.Npad;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.err = ds->err_word;
+  p.BH = BH;
+  p.N = N;
+  p.num_units = 0;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (D == 64)
+    e = causal ? launch_bwd<64, true>(tq, tk, tv, tdo, p, o, dout, lse, lse2, delta,
+                                      ds->num_sms, s)
+               : launch_bwd<64, false>(tq, tk, tv, tdo, p, o, dout, lse, lse2, delta,
+                                       ds->num_sms, s);
+  else
+    e = causal ? launch_bwd<128, true>(tq, tk, tv, tdo, p, o, dout, lse, lse2, delta,
+                                       ds->num_sms, s)
+               : launch_bwd<128, false>(tq, tk, tv, tdo, p, o, dout, lse, lse2, delta,
+                                        ds->num_sms, s);
+  return e == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 
 // ---------------------------------------------------------------- GEMM

@@ -1,0 +1,655 @@
+// tk_attn_bwd.cuh -- the attention backward pass on GB300 (sm_103a): dQ, dK
+// and dV of O = softmax(scale Q K^T [+ causal mask]) V for a given dO, from
+// the forward's O and LSE.
+//
+// The pages report causal and non-causal FlashAttention backward kernels in
+// ThunderKittens (the comment thread of the Spanish news page,
+// es.news.hada.io topic 14783; the paper summary "ThunderKittens: Simple,
+// Fast, and Adorable AI Kernels", shd-paper.top, abstract) but print none.
+// The arithmetic is the chain rule through the forward definition:
+//   P_ij  = exp(scale q_i.k_j - LSE_i)           (recomputed, masked -> 0)
+//   dV_j  = sum_i P_ij dO_i
+//   dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - delta_i),  delta_i = sum_d dO_id O_id
+//   dK_j  = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
+//
+// Three kernels, one stream, no atomics:
+//   prep   delta_i and LSE_i log2(e) into a workspace padded to whole tiles
+//   dkdv   one unit = (slice, 128-key tile j): K_j, V_j stay in shared memory
+//          while every 128-query tile i streams through a ring.  S^T = K Q^T
+//          and dP^T = V dO^T go to TMEM; eight elementwise warps turn them
+//          into bf16 P^T and dS^T in place, and two tcgen05 MMAs with A read
+//          from TMEM accumulate dV += P^T dO and dK += dS^T Q in TMEM.
+//   dq     one unit = (slice, 128-query tile i): Q_i, dO_i stay while the
+//          K/V tiles stream; S = Q K^T and dP = dO V^T in TMEM, bf16 dS in
+//          place, dQ += dS K in TMEM.
+// dkdv and dq each recompute S and dP, so the pass runs 7 tile products per
+// (query tile, key tile) pair instead of the 5 an atomic dQ update needs; in
+// exchange no fp32 dQ buffer and no reduction traffic.
+//
+// Tiles use the forward's layout (128 rows, 64-column chunks with the
+// 128-byte swizzle, TMA from [B*H, N, D] tensor maps), so the forward's
+// S-product issue helper serves S^T, dP^T, S and dP alike; the gradient
+// products read their B operand (dO, Q or K) MN-major like the forward's V.
+#pragma once
+
+#include "tk_attn_fwd.cuh"
+
+namespace tkattn {
+
+struct BwdParams {
+  __nv_bfloat16 *dq, *dk, *dv;  // [BH, N, D] outputs
+  const float *lse2;            // [BH, Npad] LSE * log2(e), zero past N
+  const float *delta;           // [BH, Npad] rowsum(dO * O), zero past N
+  int *err;                     // device error word
+  int BH, N, Npad, nt;          // nt = Npad / 128 tiles per slice
+  int num_units;
+  float scale, scale_log2;      // scale and scale * log2(e)
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = 128 * 128;   // 128 rows x 128 B
+  static constexpr int kStages = D == 128 ? 2 : 4;  // ring depth in tile pairs
+  static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static constexpr int kThreads = 320;            // 8 elementwise warps, producer, MMA
+  // TMEM columns: S (or S^T), dP (or dP^T), and the D-wide accumulators
+  static constexpr uint32_t kColS = 0, kColdP = 128, kColA = 256, kColB = 256 + D;
+};
+
+template <int kStages>
+struct BwdShared {
+  uint64_t fix_full, fix_empty;  // the unit's resident pair landed / released
+  uint64_t ring_full[kStages], ring_empty[kStages];
+  uint64_t s_full;               // S and dP of a step complete       (commit)
+  uint64_t p_full;               // bf16 P / dS of a step in TMEM      (8 warps)
+  uint64_t acc_full, acc_empty;  // unit's accumulators done / read    (commit / 8 warps)
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  alignas(128) float vec[kStages][2][128];  // dkdv: LSE log2(e), delta of the ring's query tile
+};
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// D (+)= A[tmem, bf16 pairs] B[smem, MN-major] over 128 rows of K: 16 per MMA.
+// The elementwise warps leave the 128 K-columns' bf16 pairs in two halves,
+// columns [0, 32) and [64, 96) of the A region.
+__device__ __forceinline__ void issue_grad(uint32_t tD, uint32_t tA, uint32_t b_lo, uint32_t dhi,
+                                           uint32_t idG, uint32_t acc) {
+  umma_ts_w_rt(tD, tA, b_lo, dhi, idG, acc);
+#pragma unroll
+  for (int kk = 1; kk < 8; ++kk)
+    umma_ts_w<1>(tD, tA + 64 * (kk >> 2) + 8 * (kk & 3), b_lo + kk * (2048 >> 4), dhi, idG);
+}
+
+// ---------------------------------------------------------------- prep
+
+constexpr int kPrepWarps = 8;
+
+// delta = rowsum(dO * O) in fp32 and LSE * log2(e), one warp per padded row;
+// rows past N get zeros.
+template <int D>
+__global__ void __launch_bounds__(kPrepWarps * 32)
+    tk_attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o,
+                            const __nv_bfloat16 *__restrict__ dout,
+                            const float *__restrict__ lse, float *__restrict__ lse2,
+                            float *__restrict__ delta, int N, int Npad, long long rows) {
+  const long long row = (long long)blockIdx.x * kPrepWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const long long bh = row / Npad;
+  const int i = (int)(row - bh * Npad);
+  float acc = 0.f, l2 = 0.f;
+  if (i < N) {
+    const size_t base = ((size_t)bh * N + i) * D + lane * (D / 32);
+    if constexpr (D == 128) {
+      const uint2 a = *reinterpret_cast<const uint2 *>(o + base);
+      const uint2 b = *reinterpret_cast<const uint2 *>(dout + base);
+      const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        acc = fmaf(__uint_as_float(av[t] << 16), __uint_as_float(bv[t] << 16), acc);
+        acc = fmaf(__uint_as_float(av[t] & 0xffff0000u), __uint_as_float(bv[t] & 0xffff0000u),
+                   acc);
+      }
+    } else {
+      const uint32_t a = *reinterpret_cast<const uint32_t *>(o + base);
+      const uint32_t b = *reinterpret_cast<const uint32_t *>(dout + base);
+      acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
+      acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, d);
+    l2 = lse[bh * N + i] * 1.4426950408889634f;
+  }
+  if (lane == 0) {
+    lse2[row] = l2;
+    delta[row] = acc;
+  }
+}
+
+// ---------------------------------------------------------------- shared parts
+
+// Units.  dkdv: u -> (slice, key tile j); non-causal slice-major (a slice's
+// key tiles share its Q/dO in L2), causal longest first (j ascending: tile j
+// meets nt - j query tiles).  dq: u -> (slice, query tile i); causal longest
+// first (i descending: tile i meets i + 1 key tiles).
+template <bool kCausal>
+__device__ __forceinline__ void dkdv_unit(const BwdParams &p, int u, int &bh, int &j, int &i0,
+                                          int &n) {
+  if (kCausal) {
+    j = u / p.BH;
+    bh = u - j * p.BH;
+    i0 = j;
+    n = p.nt - j;
+  } else {
+    bh = u / p.nt;
+    j = u - bh * p.nt;
+    i0 = 0;
+    n = p.nt;
+  }
+}
+
+template <bool kCausal>
+__device__ __forceinline__ void dq_unit(const BwdParams &p, int u, int &bh, int &i, int &n) {
+  if (kCausal) {
+    const int r = u / p.BH;
+    bh = u - r * p.BH;
+    i = p.nt - 1 - r;
+    n = i + 1;
+  } else {
+    bh = u / p.nt;
+    i = u - bh * p.nt;
+    n = p.nt;
+  }
+}
+
+// ---------------------------------------------------------------- dK, dV
+
+template <int D, bool kCausal>
+__global__ void __launch_bounds__(320, 1)
+    tk_attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BwdShared<C::kStages> sb;
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sK = smem, *sV = smem + C::kTileBytes, *ring = smem + 2 * C::kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int *abort_flag = &sb.abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&sb.fix_full, 1);
+    mbar_init(&sb.fix_empty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&sb.ring_full[s], 1);
+      mbar_init(&sb.ring_empty[s], 1);
+    }
+    mbar_init(&sb.s_full, 1);
+    mbar_init(&sb.p_full, 8);
+    mbar_init(&sb.acc_full, 1);
+    mbar_init(&sb.acc_empty, 8);
+    mbar_init(&sb.mma_done, 1);
+    sb.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&sb.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sb.tmem_base;
+  auto fail = [&]() {
+    sb.abort = 1;
+    atomicCAS(p.err, 0, kDevErrTimeout);
+  };
+
+  if (warp < 8) {
+    // ---------------------------------------------------------- elementwise
+    const int qd = warp & 3, h = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const int r = qd * 32 + lane;  // key row within the tile = TMEM lane
+    uint32_t it = 0, gs = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      int bh, j, i0, n;
+      dkdv_unit<kCausal>(p, u, bh, j, i0, n);
+      const int kj = j * 128 + r;
+#pragma unroll 1
+      for (int st = 0; st < n; ++st, ++it, ++gs) {
+        const int i = i0 + st;
+        const uint32_t s = it % C::kStages;
+        if (!mbar_wait(&sb.s_full, gs & 1, abort_flag) ||
+            !mbar_wait(&sb.ring_full[s], (it / C::kStages) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const bool edge = (kCausal && i == j) || (i * 128 + 128 > p.N);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          uint32_t sv[32], dv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kColS + col0, sv);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
+          tmem_wait_ld();
+          const float *L = sb.vec[s][0] + col0;
+          const float *Dl = sb.vec[s][1] + col0;
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            reg_barrier(sv[t]);
+            reg_barrier(sv[t + 1]);
+            reg_barrier(dv[t]);
+            reg_barrier(dv[t + 1]);
+            float p0 = ex2_approx(fmaf(__uint_as_float(sv[t]), p.scale_log2, -L[t]));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sv[t + 1]), p.scale_log2, -L[t + 1]));
+            if (edge) {
+              const int qi = i * 128 + col0 + t;
+              if ((kCausal && qi < kj) || qi >= p.N) p0 = 0.f;
+              if ((kCausal && qi + 1 < kj) || qi + 1 >= p.N) p1 = 0.f;
+            }
+            const float d0 = p0 * (__uint_as_float(dv[t]) - Dl[t]);
+            const float d1 = p1 * (__uint_as_float(dv[t + 1]) - Dl[t + 1]);
+            pk[t >> 1] = pack_bf16x2(p0, p1);
+            dk[t >> 1] = pack_bf16x2(d0, d1);
+          }
+          tmem_st_32x32b_x16(tmem + lane_off + C::kColS + 64 * h + 16 * c, pk);
+          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sb.p_full);
+      }
+      if (!ok) break;
+      // ---- epilogue: dV and scale * dK of this key tile, rows < N
+      if (!mbar_wait(&sb.acc_full, uc & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc_fence_after_sync();
+      const bool valid = kj < p.N;
+      const size_t row_off = ((size_t)bh * p.N + (valid ? kj : 0)) * D;
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        const uint32_t col = g ? C::kColB : C::kColA;
+        __nv_bfloat16 *dst = (g ? p.dk : p.dv) + row_off;
+        const float mul = g ? p.scale : 1.f;
+#pragma unroll 1
+        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+          uint32_t rv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + col + c0, rv);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            reg_barrier(rv[t]);
+            reg_barrier(rv[t + 1]);
+            pk[t >> 1] =
+                pack_bf16x2(__uint_as_float(rv[t]) * mul, __uint_as_float(rv[t + 1]) * mul);
+          }
+          if (valid) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              *reinterpret_cast<uint4 *>(dst + c0 + 8 * t) =
+                  make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb.acc_empty);
+    }
+  } else if (warp == 8 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    uint32_t it = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      int bh, j, i0, n;
+      dkdv_unit<kCausal>(p, u, bh, j, i0, n);
+      if (uc > 0 && !mbar_wait(&sb.fix_empty, (uc - 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      mbar_arrive_expect_tx(&sb.fix_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(sK + c * C::kChunkBytes, &tm_k, &sb.fix_full, c * 64, j * 128, bh);
+        tma_load_3d(sV + c * C::kChunkBytes, &tm_v, &sb.fix_full, c * 64, j * 128, bh);
+      }
+      for (int st = 0; st < n; ++st, ++it) {
+        const int i = i0 + st;
+        const uint32_t s = it % C::kStages;
+        if (it >= (uint32_t)C::kStages &&
+            !mbar_wait(&sb.ring_empty[s], ((it / C::kStages) - 1) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        uint8_t *sQ = ring + s * 2 * C::kTileBytes, *sdO = sQ + C::kTileBytes;
+        mbar_arrive_expect_tx(&sb.ring_full[s], 2 * C::kTileBytes + 1024);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(sQ + c * C::kChunkBytes, &tm_q, &sb.ring_full[s], c * 64, i * 128, bh);
+          tma_load_3d(sdO + c * C::kChunkBytes, &tm_do, &sb.ring_full[s], c * 64, i * 128, bh);
+        }
+        const size_t vo = (size_t)bh * p.Npad + (size_t)i * 128;
+        bulk_load(sb.vec[s][0], p.lse2 + vo, 512, &sb.ring_full[s]);
+        bulk_load(sb.vec[s][1], p.delta + vo, 512, &sb.ring_full[s]);
+      }
+    }
+    // copies still in flight land before the CTA can exit
+    for (int i = 0; i < 200 && !ok; ++i) __nanosleep(1000);
+  } else if (warp == 9 && lane == 0) {
+    // ---------------------------------------------------------- MMA issue
+    constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);
+    constexpr uint32_t idG = idesc_f32acc(true, 128, D, false, true);
+    const uint32_t dhi = sdesc_sw128_hi(1024);
+    const uint32_t k_lo = sdesc_sw128_lo(smem_addr(sK), 16);
+    const uint32_t v_lo = sdesc_sw128_lo(smem_addr(sV), 16);
+    uint32_t it = 0, gs = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      int bh, j, i0, n;
+      dkdv_unit<kCausal>(p, u, bh, j, i0, n);
+      if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc_fence_after_sync();
+      for (int st = 0; st < n; ++st, ++it, ++gs) {
+        const uint32_t s = it % C::kStages;
+        if (!mbar_wait(&sb.ring_full[s], (it / C::kStages) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t sq = smem_addr(ring + s * 2 * C::kTileBytes);
+        const uint32_t sdo = sq + C::kTileBytes;
+        // S^T = K Q^T and dP^T = V dO^T (rows: keys; columns: queries)
+        issue_s<D>(tmem + C::kColS, k_lo, sdesc_sw128_lo(sq, 16), dhi, idS);
+        issue_s<D>(tmem + C::kColdP, v_lo, sdesc_sw128_lo(sdo, 16), dhi, idS);
+        umma_commit(&sb.s_full);
+        // the epilogue has read the previous unit's accumulators
+        if (st == 0 && uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&sb.p_full, gs & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // dV += P^T dO and dK += dS^T Q (B operands MN-major)
+        const uint32_t acc = st > 0 ? 1u : 0u;
+        issue_grad(tmem + C::kColA, tmem + C::kColS, sdesc_sw128_lo(sdo, C::kChunkBytes), dhi,
+                   idG, acc);
+        issue_grad(tmem + C::kColB, tmem + C::kColdP, sdesc_sw128_lo(sq, C::kChunkBytes), dhi,
+                   idG, acc);
+        umma_commit(&sb.ring_empty[s]);
+      }
+      if (!ok) break;
+      umma_commit(&sb.acc_full);
+      umma_commit(&sb.fix_empty);
+    }
+    umma_commit(&sb.mma_done);
+    int never = 0;
+    mbar_wait(&sb.mma_done, 0, &never);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+
+template <int D, bool kCausal>
+__global__ void __launch_bounds__(320, 1)
+    tk_attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BwdShared<C::kStages> sb;
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sQ = smem, *sdO = smem + C::kTileBytes, *ring = smem + 2 * C::kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int *abort_flag = &sb.abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&sb.fix_full, 1);
+    mbar_init(&sb.fix_empty, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&sb.ring_full[s], 1);
+      mbar_init(&sb.ring_empty[s], 1);
+    }
+    mbar_init(&sb.s_full, 1);
+    mbar_init(&sb.p_full, 8);
+    mbar_init(&sb.acc_full, 1);
+    mbar_init(&sb.acc_empty, 8);
+    mbar_init(&sb.mma_done, 1);
+    sb.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&sb.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sb.tmem_base;
+  auto fail = [&]() {
+    sb.abort = 1;
+    atomicCAS(p.err, 0, kDevErrTimeout);
+  };
+
+  if (warp < 8) {
+    // ---------------------------------------------------------- elementwise
+    const int qd = warp & 3, h = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
+    uint32_t gs = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      int bh, i, n;
+      dq_unit<kCausal>(p, u, bh, i, n);
+      const int qi = i * 128 + r;
+      const size_t vo = (size_t)bh * p.Npad + qi;
+      const float l2 = p.lse2[vo], dl = p.delta[vo];
+#pragma unroll 1
+      for (int j = 0; j < n; ++j, ++gs) {
+        if (!mbar_wait(&sb.s_full, gs & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const bool edge = (kCausal && j == i) || (j * 128 + 128 > p.N);
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          uint32_t sv[32], dv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kColS + col0, sv);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
+          tmem_wait_ld();
+          uint32_t dk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            reg_barrier(sv[t]);
+            reg_barrier(sv[t + 1]);
+            reg_barrier(dv[t]);
+            reg_barrier(dv[t + 1]);
+            float p0 = ex2_approx(fmaf(__uint_as_float(sv[t]), p.scale_log2, -l2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sv[t + 1]), p.scale_log2, -l2));
+            if (edge) {
+              const int kj = j * 128 + col0 + t;
+              if ((kCausal && kj > qi) || kj >= p.N) p0 = 0.f;
+              if ((kCausal && kj + 1 > qi) || kj + 1 >= p.N) p1 = 0.f;
+            }
+            dk[t >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[t]) - dl),
+                                     p1 * (__uint_as_float(dv[t + 1]) - dl));
+          }
+          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sb.p_full);
+      }
+      if (!ok) break;
+      // ---- epilogue: scale * dQ of this query tile, rows < N
+      if (!mbar_wait(&sb.acc_full, uc & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc_fence_after_sync();
+      const bool valid = qi < p.N;
+      __nv_bfloat16 *dst = p.dq + ((size_t)bh * p.N + (valid ? qi : 0)) * D;
+#pragma unroll 1
+      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+        uint32_t rv[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + C::kColA + c0, rv);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          reg_barrier(rv[t]);
+          reg_barrier(rv[t + 1]);
+          pk[t >> 1] = pack_bf16x2(__uint_as_float(rv[t]) * p.scale,
+                                   __uint_as_float(rv[t + 1]) * p.scale);
+        }
+        if (valid) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            *reinterpret_cast<uint4 *>(dst + c0 + 8 * t) =
+                make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb.acc_empty);
+    }
+  } else if (warp == 8 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    uint32_t it = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      int bh, i, n;
+      dq_unit<kCausal>(p, u, bh, i, n);
+      if (uc > 0 && !mbar_wait(&sb.fix_empty, (uc - 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      mbar_arrive_expect_tx(&sb.fix_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(sQ + c * C::kChunkBytes, &tm_q, &sb.fix_full, c * 64, i * 128, bh);
+        tma_load_3d(sdO + c * C::kChunkBytes, &tm_do, &sb.fix_full, c * 64, i * 128, bh);
+      }
+      for (int j = 0; j < n; ++j, ++it) {
+        const uint32_t s = it % C::kStages;
+        if (it >= (uint32_t)C::kStages &&
+            !mbar_wait(&sb.ring_empty[s], ((it / C::kStages) - 1) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        uint8_t *sK = ring + s * 2 * C::kTileBytes, *sV = sK + C::kTileBytes;
+        mbar_arrive_expect_tx(&sb.ring_full[s], 2 * C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_3d(sK + c * C::kChunkBytes, &tm_k, &sb.ring_full[s], c * 64, j * 128, bh);
+          tma_load_3d(sV + c * C::kChunkBytes, &tm_v, &sb.ring_full[s], c * 64, j * 128, bh);
+        }
+      }
+    }
+    for (int i = 0; i < 200 && !ok; ++i) __nanosleep(1000);
+  } else if (warp == 9 && lane == 0) {
+    // ---------------------------------------------------------- MMA issue
+    constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);
+    constexpr uint32_t idG = idesc_f32acc(true, 128, D, false, true);
+    const uint32_t dhi = sdesc_sw128_hi(1024);
+    const uint32_t q_lo = sdesc_sw128_lo(smem_addr(sQ), 16);
+    const uint32_t do_lo = sdesc_sw128_lo(smem_addr(sdO), 16);
+    uint32_t it = 0, gs = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+      int bh, i, n;
+      dq_unit<kCausal>(p, u, bh, i, n);
+      if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      tc_fence_after_sync();
+      for (int j = 0; j < n; ++j, ++it, ++gs) {
+        const uint32_t s = it % C::kStages;
+        if (!mbar_wait(&sb.ring_full[s], (it / C::kStages) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t sk = smem_addr(ring + s * 2 * C::kTileBytes);
+        const uint32_t sv = sk + C::kTileBytes;
+        // S = Q K^T and dP = dO V^T (rows: queries; columns: keys)
+        issue_s<D>(tmem + C::kColS, q_lo, sdesc_sw128_lo(sk, 16), dhi, idS);
+        issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(sv, 16), dhi, idS);
+        umma_commit(&sb.s_full);
+        if (j == 0 && uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&sb.p_full, gs & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // dQ += dS K (B operand MN-major)
+        issue_grad(tmem + C::kColA, tmem + C::kColdP, sdesc_sw128_lo(sk, C::kChunkBytes), dhi,
+                   idG, j > 0 ? 1u : 0u);
+        umma_commit(&sb.ring_empty[s]);
+      }
+      if (!ok) break;
+      umma_commit(&sb.acc_full);
+      umma_commit(&sb.fix_empty);
+    }
+    umma_commit(&sb.mma_done);
+    int never = 0;
+    mbar_wait(&sb.mma_done, 0, &never);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace tkattn

@@ -19,6 +19,9 @@ them, split over keys):
 
   prefill_q256_k32k_d128  B 1, H 32, Nq 256, Nk 32768, D 128, unmasked, N(0, 1)
 
+the backward pass (tk_attn_bwd) on the shapes of n4096_d128 and n8192_d128_c,
+with the output gradient dO ~ N(0, 1) drawn after Q, K, V by draw_grad(),
+
 and one dense GEMM shape for tk_gemm_bf16 (C = A B^T):
 
   gemm_8192   M = N = K = 8192, A and B ~ N(0, 1)
@@ -133,6 +136,18 @@ def draw(shape, seed: int, dist: str = "normal", device="cpu", kv_shape=None):
     else:
         raise ValueError(f"unknown distribution {dist!r}")
     return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
+
+
+def draw_grad(shape, seed: int, device="cpu"):
+    """dO for the backward pass: N(0, 1) rounded to bf16, from a generator
+    seeded with 1000 + seed (so it never repeats the draw of Q, K, V)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 + int(seed))
+    return _randn(g, shape).to(torch.bfloat16)
+
+
+# The backward pass is measured on the forward's D = 128 shapes.
+BWD_WORKLOADS = tuple(w for w in WORKLOADS if w.name in ("n4096_d128", "n8192_d128_c"))
 
 
 @dataclass(frozen=True)

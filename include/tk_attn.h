@@ -61,7 +61,7 @@ typedef struct CUstream_st *tk_attn_stream_t;
 #define TK_ATTN_ERR_TOO_LARGE (-6)      /* tk_attn_fwd_splitkv_static: the ranges'
                                            partial results exceed its static scratch */
 
-#define TK_ATTN_VERSION 10200 /* major*10000 + minor*100 + patch */
+#define TK_ATTN_VERSION 10300 /* major*10000 + minor*100 + patch */
 
 /*
  * tk_attn_fwd -- fused attention forward, asynchronous on `stream`.
@@ -162,6 +162,47 @@ size_t tk_attn_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int D, int 
 int tk_attn_fwd_splitkv_static(const void *q, const void *k, const void *v, void *o,
                                float *lse, int B, int H, int Nq, int Nk, int D, float scale,
                                int num_splits, tk_attn_stream_t stream);
+
+/*
+ * tk_attn_bwd -- the backward pass of tk_attn_fwd: given dO = dL/dO for some
+ * loss L, the gradients
+ *
+ *   dV = P^T dO,   dS = P o (dO V^T - delta),   dQ = scale dS K,
+ *   dK = scale dS^T Q,   with P_ij = exp(scale q_i.k_j - LSE_i) (0 where
+ *   masked) and delta_i = sum_d dO_id O_id,
+ *
+ * the chain rule through the forward definition.  The ThunderKittens pages
+ * report causal and non-causal FlashAttention backward kernels (comment
+ * thread of es.news.hada.io topic 14783; the paper summary "ThunderKittens:
+ * Simple, Fast, and Adorable AI Kernels", shd-paper.top, abstract) but give
+ * no formulas; these are the calculus of the forward operation above.
+ *
+ *   q, k, v, o, dout : bf16 [B, H, N, D]   (o and lse from tk_attn_fwd on
+ *   lse              : fp32 [B, H, N]       the same q, k, v, scale, causal)
+ *   dq, dk, dv       : bf16 [B, H, N, D]   outputs
+ *   workspace        : device scratch of tk_attn_bwd_workspace_bytes(B, H, N,
+ *                      D) bytes (fp32 delta and base-2 LSE per row, padded to
+ *                      128-row tiles); overwritten, owned by the caller
+ *
+ * Same conventions as tk_attn_fwd (device memory owned by the caller,
+ * 16-byte aligned bases, asynchronous on `stream`, no allocation).  The
+ * outputs and the workspace must not overlap each other or any input
+ * (TK_ATTN_ERR_INVALID_ARG), and workspace_bytes must cover the size above.
+ * Three kernels run on the stream: the row sums, then dK/dV, then dQ.
+ */
+int tk_attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int D,
+                float scale, int causal, void *workspace, size_t workspace_bytes,
+                tk_attn_stream_t stream);
+
+/* Workspace bytes tk_attn_bwd needs (0 for invalid sizes); no GPU needed. */
+size_t tk_attn_bwd_workspace_bytes(int B, int H, int N, int D);
+
+/* The argument checks of tk_attn_bwd alone (no GPU needed). */
+int tk_attn_bwd_check_args(const void *q, const void *k, const void *v, const void *o,
+                           const float *lse, const void *dout, const void *dq, const void *dk,
+                           const void *dv, int B, int H, int N, int D, float scale,
+                           const void *workspace, size_t workspace_bytes);
 
 /*
  * tk_gemm_bf16 -- dense bf16 matrix product with fp32 accumulation:
