@@ -52,9 +52,13 @@ struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = 128 * 128;   // 128 rows x 128 B
-  static constexpr int kStages = D == 128 ? 2 : 4;  // ring depth in tile pairs
+  static constexpr int kStages = D == 128 ? 2 : 4;  // dkdv: ring depth in (Q, dO) pairs
   static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  // dq: K and V rings of their own (K is needed one step earlier than V)
+  static constexpr int kKStages = D == 128 ? 3 : 4, kVStages = D == 128 ? 2 : 4;
+  static constexpr int kDqSmemAlloc = (2 + kKStages + kVStages) * kTileBytes + 1024;
+  static constexpr uint32_t kColS1 = 384;  // dq: second S buffer
   static constexpr int kThreads = 320;            // 8 elementwise warps, producer, MMA
   // TMEM columns: S (or S^T), dP (or dP^T), and the D-wide accumulators
   static constexpr uint32_t kColS = 0, kColdP = 128, kColA = 256, kColB = 256 + D;
@@ -64,8 +68,10 @@ template <int kStages>
 struct BwdShared {
   uint64_t fix_full, fix_empty;  // the unit's resident pair landed / released
   uint64_t ring_full[kStages], ring_empty[kStages];
-  uint64_t s_full;               // S and dP of a step complete       (commit)
-  uint64_t p_full;               // bf16 P / dS of a step in TMEM      (8 warps)
+  uint64_t s_full;               // S (dkdv: S^T) of a step complete   (commit)
+  uint64_t p_full;               // bf16 P (dq: dS) of a step in TMEM  (8 warps)
+  uint64_t dp_full;              // dkdv: dP^T of a step complete      (commit)
+  uint64_t ds_full;              // dkdv: bf16 dS^T of a step in TMEM  (8 warps)
   uint64_t acc_full, acc_empty;  // unit's accumulators done / read    (commit / 8 warps)
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -177,6 +183,14 @@ __device__ __forceinline__ void dq_unit(const BwdParams &p, int u, int &bh, int 
 
 // ---------------------------------------------------------------- dK, dV
 
+// One step (key tile j, query tile i) runs as two halves so that the tensor
+// core keeps working while the elementwise warps do:
+//   MMA:  S^T_i, dP^T_i | wait P_i: dV += P^T_i dO_i, S^T_{i+1} |
+//         wait dS_i: dK += dS^T_i Q_i, dP^T_{i+1} | wait P_{i+1} ...
+//   warps: wait S^T_i: P^T_i = exp2(S^T c - L) -> TMEM (bf16)  | signal P_i
+//          wait dP^T_i: dS^T_i = P (dP^T - delta) -> TMEM      | signal dS_i
+// S^T_{i+1} overwrites P^T_i and dP^T_{i+1} overwrites dS^T_i only after the
+// MMAs that read them, because one thread issues all MMAs in order.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(320, 1)
     tk_attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -200,6 +214,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&sb.s_full, 1);
     mbar_init(&sb.p_full, 8);
+    mbar_init(&sb.dp_full, 1);
+    mbar_init(&sb.ds_full, 8);
     mbar_init(&sb.acc_full, 1);
     mbar_init(&sb.acc_empty, 8);
     mbar_init(&sb.mma_done, 1);
@@ -224,17 +240,17 @@ __global__ void __launch_bounds__(320, 1)
     const int qd = warp & 3, h = warp >> 2;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int r = qd * 32 + lane;  // key row within the tile = TMEM lane
-    uint32_t it = 0, gs = 0, uc = 0;
+    uint32_t it = 0, uc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
       int bh, j, i0, n;
       dkdv_unit<kCausal>(p, u, bh, j, i0, n);
       const int kj = j * 128 + r;
 #pragma unroll 1
-      for (int st = 0; st < n; ++st, ++it, ++gs) {
+      for (int st = 0; st < n; ++st, ++it) {
         const int i = i0 + st;
         const uint32_t s = it % C::kStages;
-        if (!mbar_wait(&sb.s_full, gs & 1, abort_flag) ||
+        if (!mbar_wait(&sb.s_full, it & 1, abort_flag) ||
             !mbar_wait(&sb.ring_full[s], (it / C::kStages) & 1, abort_flag)) {
           fail();
           ok = false;
@@ -242,22 +258,20 @@ __global__ void __launch_bounds__(320, 1)
         }
         tc_fence_after_sync();
         const bool edge = (kCausal && i == j) || (i * 128 + 128 > p.N);
-#pragma unroll 1
+        // P^T = exp2(S^T scale log2(e) - LSE_i log2(e)), masked -> 0; kept in fp32
+        float pr[64];
+#pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int col0 = 64 * h + 32 * c;
-          uint32_t sv[32], dv[32];
+          uint32_t sv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + C::kColS + col0, sv);
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
           tmem_wait_ld();
           const float *L = sb.vec[s][0] + col0;
-          const float *Dl = sb.vec[s][1] + col0;
-          uint32_t pk[16], dk[16];
+          uint32_t pk[16];
 #pragma unroll
           for (int t = 0; t < 32; t += 2) {
             reg_barrier(sv[t]);
             reg_barrier(sv[t + 1]);
-            reg_barrier(dv[t]);
-            reg_barrier(dv[t + 1]);
             float p0 = ex2_approx(fmaf(__uint_as_float(sv[t]), p.scale_log2, -L[t]));
             float p1 = ex2_approx(fmaf(__uint_as_float(sv[t + 1]), p.scale_log2, -L[t + 1]));
             if (edge) {
@@ -265,18 +279,44 @@ __global__ void __launch_bounds__(320, 1)
               if ((kCausal && qi < kj) || qi >= p.N) p0 = 0.f;
               if ((kCausal && qi + 1 < kj) || qi + 1 >= p.N) p1 = 0.f;
             }
-            const float d0 = p0 * (__uint_as_float(dv[t]) - Dl[t]);
-            const float d1 = p1 * (__uint_as_float(dv[t + 1]) - Dl[t + 1]);
+            pr[32 * c + t] = p0;
+            pr[32 * c + t + 1] = p1;
             pk[t >> 1] = pack_bf16x2(p0, p1);
-            dk[t >> 1] = pack_bf16x2(d0, d1);
           }
           tmem_st_32x32b_x16(tmem + lane_off + C::kColS + 64 * h + 16 * c, pk);
-          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sb.p_full);
+        // dS^T = P^T (dP^T - delta_i)
+        if (!mbar_wait(&sb.dp_full, it & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          uint32_t dv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
+          tmem_wait_ld();
+          const float *Dl = sb.vec[s][1] + col0;
+          uint32_t dk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            reg_barrier(dv[t]);
+            reg_barrier(dv[t + 1]);
+            dk[t >> 1] = pack_bf16x2(pr[32 * c + t] * (__uint_as_float(dv[t]) - Dl[t]),
+                                     pr[32 * c + t + 1] * (__uint_as_float(dv[t + 1]) - Dl[t + 1]));
+          }
+          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sb.ds_full);
       }
       if (!ok) break;
       // ---- epilogue: dV and scale * dK of this key tile, rows < N
@@ -364,49 +404,68 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t dhi = sdesc_sw128_hi(1024);
     const uint32_t k_lo = sdesc_sw128_lo(smem_addr(sK), 16);
     const uint32_t v_lo = sdesc_sw128_lo(smem_addr(sV), 16);
-    uint32_t it = 0, gs = 0, uc = 0;
+    uint32_t it = 0, uc = 0;
     bool ok = true;
+    auto stage_q = [&](uint32_t t) { return smem_addr(ring + (t % C::kStages) * 2 * C::kTileBytes); };
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
       int bh, j, i0, n;
       dkdv_unit<kCausal>(p, u, bh, j, i0, n);
-      if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag)) {
+      if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag) ||
+          !mbar_wait(&sb.ring_full[it % C::kStages], (it / C::kStages) & 1, abort_flag)) {
         fail();
         break;
       }
       tc_fence_after_sync();
-      for (int st = 0; st < n; ++st, ++it, ++gs) {
-        const uint32_t s = it % C::kStages;
-        if (!mbar_wait(&sb.ring_full[s], (it / C::kStages) & 1, abort_flag)) {
-          fail();
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t sq = smem_addr(ring + s * 2 * C::kTileBytes);
-        const uint32_t sdo = sq + C::kTileBytes;
-        // S^T = K Q^T and dP^T = V dO^T (rows: keys; columns: queries)
-        issue_s<D>(tmem + C::kColS, k_lo, sdesc_sw128_lo(sq, 16), dhi, idS);
-        issue_s<D>(tmem + C::kColdP, v_lo, sdesc_sw128_lo(sdo, 16), dhi, idS);
-        umma_commit(&sb.s_full);
-        // the epilogue has read the previous unit's accumulators
-        if (st == 0 && uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
-          fail();
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(&sb.p_full, gs & 1, abort_flag)) {
-          fail();
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // dV += P^T dO and dK += dS^T Q (B operands MN-major)
+      // step 0's S^T = K Q^T and dP^T = V dO^T (rows: keys; columns: queries)
+      issue_s<D>(tmem + C::kColS, k_lo, sdesc_sw128_lo(stage_q(it), 16), dhi, idS);
+      umma_commit(&sb.s_full);
+      issue_s<D>(tmem + C::kColdP, v_lo, sdesc_sw128_lo(stage_q(it) + C::kTileBytes, 16), dhi,
+                 idS);
+      umma_commit(&sb.dp_full);
+      // the epilogue has read the previous unit's accumulators
+      if (uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      for (int st = 0; st < n; ++st, ++it) {
+        const uint32_t sq = stage_q(it), sdo = sq + C::kTileBytes;
         const uint32_t acc = st > 0 ? 1u : 0u;
+        if (!mbar_wait(&sb.p_full, it & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // dV += P^T dO (B operand MN-major), then the next step's S^T
         issue_grad(tmem + C::kColA, tmem + C::kColS, sdesc_sw128_lo(sdo, C::kChunkBytes), dhi,
                    idG, acc);
+        const bool more = st + 1 < n;
+        if (more) {
+          if (!mbar_wait(&sb.ring_full[(it + 1) % C::kStages], ((it + 1) / C::kStages) & 1,
+                         abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s<D>(tmem + C::kColS, k_lo, sdesc_sw128_lo(stage_q(it + 1), 16), dhi, idS);
+          umma_commit(&sb.s_full);
+        }
+        if (!mbar_wait(&sb.ds_full, it & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        // dK += dS^T Q, then the next step's dP^T
         issue_grad(tmem + C::kColB, tmem + C::kColdP, sdesc_sw128_lo(sq, C::kChunkBytes), dhi,
                    idG, acc);
-        umma_commit(&sb.ring_empty[s]);
+        umma_commit(&sb.ring_empty[it % C::kStages]);
+        if (more) {
+          issue_s<D>(tmem + C::kColdP, v_lo, sdesc_sw128_lo(stage_q(it + 1) + C::kTileBytes, 16),
+                     dhi, idS);
+          umma_commit(&sb.dp_full);
+        }
       }
       if (!ok) break;
       umma_commit(&sb.acc_full);
@@ -426,6 +485,24 @@ __global__ void __launch_bounds__(320, 1)
 
 // ---------------------------------------------------------------- dQ
 
+template <int kKStages, int kVStages>
+struct DqShared {
+  uint64_t fix_full, fix_empty;  // the unit's Q_i, dO_i landed / released
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full;               // S and dP of a step complete   (commit)
+  uint64_t p_full;               // bf16 dS of a step in TMEM     (8 warps)
+  uint64_t acc_full, acc_empty;  // dQ done / read                (commit / 8 warps)
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Per step j (key tile j) the MMA thread issues S_{j+1} = Q K_{j+1}^T into
+// the other S buffer before it waits for the elementwise warps' dS_j, so the
+// tensor core computes the next scores while the warps work:
+//   S_{j+1} | wait dS_j: dQ += dS_j K_j, dP_{j+1} = dO V_{j+1}^T | wait dS_{j+1}
+// dP_{j+1} overwrites dS_j only after the MMA that reads it (in-order issue).
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(320, 1)
     tk_attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -433,19 +510,25 @@ __global__ void __launch_bounds__(320, 1)
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using C = BwdCfg<D>;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ BwdShared<C::kStages> sb;
+  __shared__ DqShared<KS, VS> sb;
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *sQ = smem, *sdO = smem + C::kTileBytes, *ring = smem + 2 * C::kTileBytes;
+  uint8_t *sQ = smem, *sdO = smem + C::kTileBytes;
+  uint8_t *kring = smem + 2 * C::kTileBytes, *vring = kring + KS * C::kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int *abort_flag = &sb.abort;
   if (threadIdx.x == 0) {
     mbar_init(&sb.fix_full, 1);
     mbar_init(&sb.fix_empty, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&sb.ring_full[s], 1);
-      mbar_init(&sb.ring_empty[s], 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&sb.k_full[s], 1);
+      mbar_init(&sb.k_empty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&sb.v_full[s], 1);
+      mbar_init(&sb.v_empty[s], 1);
     }
     mbar_init(&sb.s_full, 1);
     mbar_init(&sb.p_full, 8);
@@ -467,13 +550,14 @@ __global__ void __launch_bounds__(320, 1)
     sb.abort = 1;
     atomicCAS(p.err, 0, kDevErrTimeout);
   };
+  auto s_col = [](uint32_t step) { return (step & 1) ? C::kColS1 : C::kColS; };
 
   if (warp < 8) {
     // ---------------------------------------------------------- elementwise
     const int qd = warp & 3, h = warp >> 2;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
-    uint32_t gs = 0, uc = 0;
+    uint32_t it = 0, uc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
       int bh, i, n;
@@ -482,19 +566,20 @@ __global__ void __launch_bounds__(320, 1)
       const size_t vo = (size_t)bh * p.Npad + qi;
       const float l2 = p.lse2[vo], dl = p.delta[vo];
 #pragma unroll 1
-      for (int j = 0; j < n; ++j, ++gs) {
-        if (!mbar_wait(&sb.s_full, gs & 1, abort_flag)) {
+      for (int j = 0; j < n; ++j, ++it) {
+        if (!mbar_wait(&sb.s_full, it & 1, abort_flag)) {
           fail();
           ok = false;
           break;
         }
         tc_fence_after_sync();
+        const uint32_t tS = tmem + lane_off + s_col(it);
         const bool edge = (kCausal && j == i) || (j * 128 + 128 > p.N);
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           const int col0 = 64 * h + 32 * c;
           uint32_t sv[32], dv[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kColS + col0, sv);
+          tmem_ld_32x32b_x32(tS + col0, sv);
           tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
           tmem_wait_ld();
           uint32_t dk[16];
@@ -572,20 +657,27 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(sdO + c * C::kChunkBytes, &tm_do, &sb.fix_full, c * 64, i * 128, bh);
       }
       for (int j = 0; j < n; ++j, ++it) {
-        const uint32_t s = it % C::kStages;
-        if (it >= (uint32_t)C::kStages &&
-            !mbar_wait(&sb.ring_empty[s], ((it / C::kStages) - 1) & 1, abort_flag)) {
+        const uint32_t ks = it % KS, vs = it % VS;
+        if (it >= (uint32_t)KS && !mbar_wait(&sb.k_empty[ks], ((it / KS) - 1) & 1, abort_flag)) {
           fail();
           ok = false;
           break;
         }
-        uint8_t *sK = ring + s * 2 * C::kTileBytes, *sV = sK + C::kTileBytes;
-        mbar_arrive_expect_tx(&sb.ring_full[s], 2 * C::kTileBytes);
+        uint8_t *sK = kring + ks * C::kTileBytes;
+        mbar_arrive_expect_tx(&sb.k_full[ks], C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(sK + c * C::kChunkBytes, &tm_k, &sb.ring_full[s], c * 64, j * 128, bh);
-          tma_load_3d(sV + c * C::kChunkBytes, &tm_v, &sb.ring_full[s], c * 64, j * 128, bh);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sK + c * C::kChunkBytes, &tm_k, &sb.k_full[ks], c * 64, j * 128, bh);
+        if (it >= (uint32_t)VS && !mbar_wait(&sb.v_empty[vs], ((it / VS) - 1) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
         }
+        uint8_t *sV = vring + vs * C::kTileBytes;
+        mbar_arrive_expect_tx(&sb.v_full[vs], C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sV + c * C::kChunkBytes, &tm_v, &sb.v_full[vs], c * 64, j * 128, bh);
       }
     }
     for (int i = 0; i < 200 && !ok; ++i) __nanosleep(1000);
@@ -596,45 +688,62 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t dhi = sdesc_sw128_hi(1024);
     const uint32_t q_lo = sdesc_sw128_lo(smem_addr(sQ), 16);
     const uint32_t do_lo = sdesc_sw128_lo(smem_addr(sdO), 16);
-    uint32_t it = 0, gs = 0, uc = 0;
+    auto k_addr = [&](uint32_t t) { return smem_addr(kring + (t % KS) * C::kTileBytes); };
+    auto v_addr = [&](uint32_t t) { return smem_addr(vring + (t % VS) * C::kTileBytes); };
+    uint32_t it = 0, uc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
       int bh, i, n;
       dq_unit<kCausal>(p, u, bh, i, n);
-      if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag)) {
+      // step 0: S_0 = Q K_0^T and dP_0 = dO V_0^T (rows: queries; columns: keys)
+      if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag) ||
+          !mbar_wait(&sb.k_full[it % KS], (it / KS) & 1, abort_flag) ||
+          !mbar_wait(&sb.v_full[it % VS], (it / VS) & 1, abort_flag)) {
         fail();
         break;
       }
       tc_fence_after_sync();
-      for (int j = 0; j < n; ++j, ++it, ++gs) {
-        const uint32_t s = it % C::kStages;
-        if (!mbar_wait(&sb.ring_full[s], (it / C::kStages) & 1, abort_flag)) {
-          fail();
-          ok = false;
-          break;
+      issue_s<D>(tmem + s_col(it), q_lo, sdesc_sw128_lo(k_addr(it), 16), dhi, idS);
+      issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(v_addr(it), 16), dhi, idS);
+      umma_commit(&sb.s_full);
+      umma_commit(&sb.v_empty[it % VS]);
+      if (uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      for (int j = 0; j < n; ++j, ++it) {
+        const bool more = j + 1 < n;
+        if (more) {
+          // the next scores, into the other S buffer, while the warps work
+          if (!mbar_wait(&sb.k_full[(it + 1) % KS], ((it + 1) / KS) & 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s<D>(tmem + s_col(it + 1), q_lo, sdesc_sw128_lo(k_addr(it + 1), 16), dhi, idS);
         }
-        tc_fence_after_sync();
-        const uint32_t sk = smem_addr(ring + s * 2 * C::kTileBytes);
-        const uint32_t sv = sk + C::kTileBytes;
-        // S = Q K^T and dP = dO V^T (rows: queries; columns: keys)
-        issue_s<D>(tmem + C::kColS, q_lo, sdesc_sw128_lo(sk, 16), dhi, idS);
-        issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(sv, 16), dhi, idS);
-        umma_commit(&sb.s_full);
-        if (j == 0 && uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
-          fail();
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(&sb.p_full, gs & 1, abort_flag)) {
+        if (!mbar_wait(&sb.p_full, it & 1, abort_flag)) {
           fail();
           ok = false;
           break;
         }
         tc_fence_after_sync();
         // dQ += dS K (B operand MN-major)
-        issue_grad(tmem + C::kColA, tmem + C::kColdP, sdesc_sw128_lo(sk, C::kChunkBytes), dhi,
-                   idG, j > 0 ? 1u : 0u);
-        umma_commit(&sb.ring_empty[s]);
+        issue_grad(tmem + C::kColA, tmem + C::kColdP, sdesc_sw128_lo(k_addr(it), C::kChunkBytes),
+                   dhi, idG, j > 0 ? 1u : 0u);
+        umma_commit(&sb.k_empty[it % KS]);
+        if (more) {
+          if (!mbar_wait(&sb.v_full[(it + 1) % VS], ((it + 1) / VS) & 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(v_addr(it + 1), 16), dhi, idS);
+          umma_commit(&sb.s_full);
+          umma_commit(&sb.v_empty[(it + 1) % VS]);
+        }
       }
       if (!ok) break;
       umma_commit(&sb.acc_full);

@@ -3,6 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tk|reference]
                     [--workload NAME] [--all-workloads]
 
+`--workload bwd_n4096_d128` (or bwd_<any forward workload>) times the backward
+pass, tk_attn_bwd, with the forward's outputs computed beforehand.
+
 `--workload gemm_8192` times the library's bf16 GEMM (tk_gemm_bf16, C = A B^T,
 M = N = K = 8192) instead, with cuBLAS (torch.matmul) on the same operands
 beside it.
@@ -302,6 +305,57 @@ def time_gemm(gw, steps: int, warmup: int, device, cublas: bool = True):
     return ms, (run(theirs) if cublas else None)
 
 
+def time_bwd(w, steps: int, warmup: int, device):
+    """CUDA-event times of `steps` tk_attn_bwd calls (three kernels each: row
+    sums, dK/dV, dQ), L2 flushed before each; the forward's O and LSE are
+    computed once beforehand, outside the timed region."""
+    import torch
+
+    from attention_forward_tk_gb300 import api
+    from attention_forward_tk_gb300.inputs import draw_grad, workload_inputs
+
+    q, k, v = workload_inputs(w, device=device)
+    do = draw_grad(w.shape, w.seed, device=device)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = api.tk_attn_bwd_workspace_bytes(w.B, w.H, w.N, w.D)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    st = api.tk_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                         w.B, w.H, w.N, w.D, w.scale, int(w.causal), sh)
+    if st:
+        raise RuntimeError(api.tk_attn_status_string(st))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N, w.D, w.scale,
+            int(w.causal), ws.data_ptr(), need, sh)
+    for _ in range(warmup):
+        flush.zero_()
+        st = api.tk_attn_bwd(*args)
+        if st:
+            raise RuntimeError(api.tk_attn_status_string(st))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        api.tk_attn_bwd(*args)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    if api.tk_attn_last_device_error(sh) != 0:
+        raise RuntimeError("device-side barrier timeout in tk_attn_bwd")
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+def bwd_flops(w) -> float:
+    """The backward's five tile products per (query, key) pair against the
+    forward's two: 2.5 x the forward FLOPs (the kernels execute seven)."""
+    return 2.5 * w.flops
+
+
 def time_e2e(w, steps: int, warmup: int, device):
     """The same call from pinned host buffers: H2D of Q, K, V, the kernel, and
     D2H of O and LSE every step, timed with CUDA events around all of it."""
@@ -374,11 +428,13 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from attention_forward_tk_gb300.inputs import (BY_NAME, EXTRA_WORKLOADS, GEMM_BY_NAME,
-                                                   GEMM_WORKLOADS, WORKLOADS)
+    from attention_forward_tk_gb300.inputs import (BWD_WORKLOADS, BY_NAME, EXTRA_WORKLOADS,
+                                                   GEMM_BY_NAME, GEMM_WORKLOADS, WORKLOADS)
     world, rank, local = dist_env()
     if args.workload in GEMM_BY_NAME:
         return main_gemm(args, GEMM_BY_NAME[args.workload], world, rank, local)
+    if args.workload.startswith("bwd_") and args.workload[4:] in BY_NAME:
+        return main_bwd(args, BY_NAME[args.workload[4:]], world, rank, local)
     w = BY_NAME[args.workload]
 
     if args.impl == "reference":
@@ -434,6 +490,15 @@ def main():
             c = oclk.summary()
             extra[ow.name] = {"ms": round(m, 4), "tflops": round(ow.flops / m / 1e9, 1),
                               "launches": n, "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
+        for bw in BWD_WORKLOADS:
+            with ClockSampler(device.index if world == 1 else local) as oclk:
+                bms = time_bwd(bw, 20, 3, device)
+            m = statistics.median(bms)
+            c = oclk.summary()
+            extra["bwd_" + bw.name] = {"ms": round(m, 4),
+                                       "tflops": round(bwd_flops(bw) / m / 1e9, 1),
+                                       "launches": 60, "sm_mhz": c["sm_mhz"],
+                                       "reasons": c["reasons"]}
         for gw in GEMM_WORKLOADS:
             with ClockSampler(device.index if world == 1 else local) as oclk:
                 gms, cms = time_gemm(gw, 100, 5, device)
@@ -508,6 +573,41 @@ def main():
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def main_bwd(args, w, world, rank, local):
+    """`--workload bwd_<forward workload>`: the backward pass (tk_attn_bwd) on
+    that workload's shape, dO ~ N(0, 1)."""
+    import torch
+
+    from attention_forward_tk_gb300.build import build_library
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    build_library()
+    with ClockSampler(device.index) as clk:
+        ms = time_bwd(w, args.steps, args.warmup, device)
+    if rank != 0:
+        return
+    peak_tf, _, peak_kind = measured_peaks()
+    t = statistics.mean(ms)
+    achieved = bwd_flops(w) / (t / 1e3) / 1e12
+    line = {
+        "metric": "attention bwd TFLOP/s (bf16, 1xGB300; 2.5x forward FLOPs)",
+        "value": round(achieved, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "bwd_" + w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                   "causal": w.causal, "flops_per_step": bwd_flops(w),
+                   "l2": "flushed (256 MB write) before every timed step"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                     "peak_kind": f"{peak_kind} dense bf16 (burst)", "traffic": None,
+                     "executed_tflops": round(1.4 * achieved, 1)},
+        "gpu_launches": 3 * args.steps,
+        "kernel_ms_median": round(statistics.median(ms), 5),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
 
 
 def main_gemm(args, gw, world, rank, local):
