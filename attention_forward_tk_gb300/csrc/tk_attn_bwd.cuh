@@ -14,7 +14,7 @@
 //   dK_j  = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
 //
 // Three kernels, one stream, no atomics:
-//   prep   delta_i and LSE_i log2(e) into a workspace padded to whole tiles
+//   prep   -delta_i and -LSE_i log2(e) into a workspace padded to whole tiles
 //   dkdv   one unit = (slice, 128-key tile j): K_j, V_j stay in shared memory
 //          while every 128-query tile i streams through a ring.  S^T = K Q^T
 //          and dP^T = V dO^T go to TMEM; eight elementwise warps turn them
@@ -39,8 +39,8 @@ namespace tkattn {
 
 struct BwdParams {
   __nv_bfloat16 *dq, *dk, *dv;  // [BH, N, D] outputs
-  const float *lse2;            // [BH, Npad] LSE * log2(e), zero past N
-  const float *delta;           // [BH, Npad] rowsum(dO * O), zero past N
+  const float *lse2;            // [BH, Npad] -LSE * log2(e), zero past N
+  const float *delta;           // [BH, Npad] -rowsum(dO * O), zero past N
   int *err;                     // device error word
   int BH, N, Npad, nt;          // nt = Npad / 128 tiles per slice
   int num_units;
@@ -76,7 +76,7 @@ struct BwdShared {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  alignas(128) float vec[kStages][2][128];  // dkdv: LSE log2(e), delta of the ring's query tile
+  alignas(128) float vec[kStages][2][128];  // dkdv: -LSE log2(e), -delta of the ring's query tile
 };
 
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
@@ -103,7 +103,8 @@ __device__ __forceinline__ void issue_grad(uint32_t tD, uint32_t tA, uint32_t b_
 
 constexpr int kPrepWarps = 8;
 
-// delta = rowsum(dO * O) in fp32 and LSE * log2(e), one warp per padded row;
+// -delta = -rowsum(dO * O) in fp32 and -LSE * log2(e), one warp per padded
+// row (negated, so the elementwise passes use them as packed f32x2 addends);
 // rows past N get zeros.
 template <int D>
 __global__ void __launch_bounds__(kPrepWarps * 32)
@@ -140,8 +141,8 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
     l2 = lse[bh * N + i] * 1.4426950408889634f;
   }
   if (lane == 0) {
-    lse2[row] = l2;
-    delta[row] = acc;
+    lse2[row] = -l2;
+    delta[row] = -acc;
   }
 }
 
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(320, 1)
     const int qd = warp & 3, h = warp >> 2;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int r = qd * 32 + lane;  // key row within the tile = TMEM lane
+    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t it = 0, uc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
@@ -259,28 +261,30 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after_sync();
         const bool edge = (kCausal && i == j) || (i * 128 + 128 > p.N);
         // P^T = exp2(S^T scale log2(e) - LSE_i log2(e)), masked -> 0; kept in fp32
-        float pr[64];
+        uint64_t pr[32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int col0 = 64 * h + 32 * c;
           uint32_t sv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + C::kColS + col0, sv);
           tmem_wait_ld();
-          const float *L = sb.vec[s][0] + col0;
+          const uint64_t *nL = reinterpret_cast<const uint64_t *>(sb.vec[s][0] + col0);
           uint32_t pk[16];
 #pragma unroll
           for (int t = 0; t < 32; t += 2) {
             reg_barrier(sv[t]);
             reg_barrier(sv[t + 1]);
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[t]), p.scale_log2, -L[t]));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[t + 1]), p.scale_log2, -L[t + 1]));
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), c2,
+                             nL[t >> 1]),
+                      a0, a1);
+            float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
             if (edge) {
               const int qi = i * 128 + col0 + t;
               if ((kCausal && qi < kj) || qi >= p.N) p0 = 0.f;
               if ((kCausal && qi + 1 < kj) || qi + 1 >= p.N) p1 = 0.f;
             }
-            pr[32 * c + t] = p0;
-            pr[32 * c + t + 1] = p1;
+            pr[16 * c + (t >> 1)] = f2_pack(p0, p1);
             pk[t >> 1] = pack_bf16x2(p0, p1);
           }
           tmem_st_32x32b_x16(tmem + lane_off + C::kColS + 64 * h + 16 * c, pk);
@@ -302,14 +306,18 @@ __global__ void __launch_bounds__(320, 1)
           uint32_t dv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
           tmem_wait_ld();
-          const float *Dl = sb.vec[s][1] + col0;
+          const uint64_t *nD = reinterpret_cast<const uint64_t *>(sb.vec[s][1] + col0);
           uint32_t dk[16];
 #pragma unroll
           for (int t = 0; t < 32; t += 2) {
             reg_barrier(dv[t]);
             reg_barrier(dv[t + 1]);
-            dk[t >> 1] = pack_bf16x2(pr[32 * c + t] * (__uint_as_float(dv[t]) - Dl[t]),
-                                     pr[32 * c + t + 1] * (__uint_as_float(dv[t + 1]) - Dl[t + 1]));
+            float d0, d1;
+            f2_unpack(f2_mul(pr[16 * c + (t >> 1)],
+                             f2_add(f2_pack(__uint_as_float(dv[t]), __uint_as_float(dv[t + 1])),
+                                    nD[t >> 1])),
+                      d0, d1);
+            dk[t >> 1] = pack_bf16x2(d0, d1);
           }
           tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
         }
@@ -557,6 +565,7 @@ __global__ void __launch_bounds__(320, 1)
     const int qd = warp & 3, h = warp >> 2;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
+    const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t it = 0, uc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
@@ -564,7 +573,8 @@ __global__ void __launch_bounds__(320, 1)
       dq_unit<kCausal>(p, u, bh, i, n);
       const int qi = i * 128 + r;
       const size_t vo = (size_t)bh * p.Npad + qi;
-      const float l2 = p.lse2[vo], dl = p.delta[vo];
+      const uint64_t nl2 = f2_pack(p.lse2[vo], p.lse2[vo]);
+      const uint64_t ndl = f2_pack(p.delta[vo], p.delta[vo]);
 #pragma unroll 1
       for (int j = 0; j < n; ++j, ++it) {
         if (!mbar_wait(&sb.s_full, it & 1, abort_flag)) {
@@ -589,15 +599,21 @@ __global__ void __launch_bounds__(320, 1)
             reg_barrier(sv[t + 1]);
             reg_barrier(dv[t]);
             reg_barrier(dv[t + 1]);
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[t]), p.scale_log2, -l2));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[t + 1]), p.scale_log2, -l2));
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), c2, nl2),
+                      a0, a1);
+            float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
             if (edge) {
               const int kj = j * 128 + col0 + t;
               if ((kCausal && kj > qi) || kj >= p.N) p0 = 0.f;
               if ((kCausal && kj + 1 > qi) || kj + 1 >= p.N) p1 = 0.f;
             }
-            dk[t >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[t]) - dl),
-                                     p1 * (__uint_as_float(dv[t + 1]) - dl));
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1),
+                             f2_add(f2_pack(__uint_as_float(dv[t]), __uint_as_float(dv[t + 1])),
+                                    ndl)),
+                      d0, d1);
+            dk[t >> 1] = pack_bf16x2(d0, d1);
           }
           tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
         }
