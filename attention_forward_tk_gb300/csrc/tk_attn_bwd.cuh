@@ -430,6 +430,9 @@ __global__ void __launch_bounds__(320, 1)
       issue_s<D>(tmem + C::kColdP, v_lo, sdesc_sw128_lo(stage_q(it) + C::kTileBytes, 16), dhi,
                  idS);
       umma_commit(&sb.dp_full);
+      // K_j and V_j are read by the S^T and dP^T products only: the last dP^T
+      // releases them, so the next unit's pair loads during this unit's tail
+      if (n == 1) umma_commit(&sb.fix_empty);
       // the epilogue has read the previous unit's accumulators
       if (uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
         fail();
@@ -473,11 +476,11 @@ __global__ void __launch_bounds__(320, 1)
           issue_s<D>(tmem + C::kColdP, v_lo, sdesc_sw128_lo(stage_q(it + 1) + C::kTileBytes, 16),
                      dhi, idS);
           umma_commit(&sb.dp_full);
+          if (st + 2 == n) umma_commit(&sb.fix_empty);
         }
       }
       if (!ok) break;
       umma_commit(&sb.acc_full);
-      umma_commit(&sb.fix_empty);
     }
     umma_commit(&sb.mma_done);
     int never = 0;
@@ -723,6 +726,9 @@ __global__ void __launch_bounds__(320, 1)
       issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(v_addr(it), 16), dhi, idS);
       umma_commit(&sb.s_full);
       umma_commit(&sb.v_empty[it % VS]);
+      // Q_i and dO_i are read by the S and dP products only: the last dP
+      // releases them, so the next unit's pair loads during this unit's tail
+      if (n == 1) umma_commit(&sb.fix_empty);
       if (uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
         fail();
         break;
@@ -759,11 +765,11 @@ __global__ void __launch_bounds__(320, 1)
           issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(v_addr(it + 1), 16), dhi, idS);
           umma_commit(&sb.s_full);
           umma_commit(&sb.v_empty[(it + 1) % VS]);
+          if (j + 2 == n) umma_commit(&sb.fix_empty);
         }
       }
       if (!ok) break;
       umma_commit(&sb.acc_full);
-      umma_commit(&sb.fix_empty);
     }
     umma_commit(&sb.mma_done);
     int never = 0;
