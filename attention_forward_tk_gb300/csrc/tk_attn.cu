@@ -532,7 +532,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   tk_attn_bwd_dkdv_kernel<D, kCausal>
       <<<grid, BwdCfg<D>::kThreads, BwdCfg<D>::kSmemAlloc, s>>>(tq, tk, tv, tdo, p);
   tk_attn_bwd_dq_kernel<D, kCausal>
-      <<<grid, BwdCfg<D>::kThreads, BwdCfg<D>::kDqSmemAlloc, s>>>(tq, tk, tv, tdo, p);
+      <<<grid, BwdCfg<D>::kDqThreads, BwdCfg<D>::kDqSmemAlloc, s>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 

@@ -59,6 +59,7 @@ struct BwdCfg {
   static constexpr int kKStages = D == 128 ? 3 : 4, kVStages = D == 128 ? 2 : 4;
   static constexpr int kDqSmemAlloc = (2 + kKStages + kVStages) * kTileBytes + 1024;
   static constexpr uint32_t kColS1 = 384;  // dq: second S buffer
+  static constexpr int kDqThreads = 576;   // dq: 16 elementwise warps, producer, MMA
   static constexpr int kThreads = 320;            // 8 elementwise warps, producer, MMA
   // TMEM columns: S (or S^T), dP (or dP^T), and the D-wide accumulators
   static constexpr uint32_t kColS = 0, kColdP = 128, kColA = 256, kColB = 256 + D;
@@ -91,12 +92,17 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // D (+)= A[tmem, bf16 pairs] B[smem, MN-major] over 128 rows of K: 16 per MMA.
 // The elementwise warps leave the 128 K-columns' bf16 pairs in two halves,
 // columns [0, 32) and [64, 96) of the A region.
+// With kParts = 4 (sixteen elementwise warps) the pairs sit in four quarters,
+// columns [0, 16), [32, 48), [64, 80) and [96, 112).
+template <int kParts = 2>
 __device__ __forceinline__ void issue_grad(uint32_t tD, uint32_t tA, uint32_t b_lo, uint32_t dhi,
                                            uint32_t idG, uint32_t acc) {
+  constexpr int kPer = 8 / kParts;  // MMAs (16 K-columns each) per part
   umma_ts_w_rt(tD, tA, b_lo, dhi, idG, acc);
 #pragma unroll
   for (int kk = 1; kk < 8; ++kk)
-    umma_ts_w<1>(tD, tA + 64 * (kk >> 2) + 8 * (kk & 3), b_lo + kk * (2048 >> 4), dhi, idG);
+    umma_ts_w<1>(tD, tA + (128 / kParts) * (kk / kPer) + 8 * (kk % kPer),
+                 b_lo + kk * (2048 >> 4), dhi, idG);
 }
 
 // ---------------------------------------------------------------- prep
@@ -509,13 +515,14 @@ struct DqShared {
   int abort;
 };
 
-// Per step j (key tile j) the MMA thread issues S_{j+1} = Q K_{j+1}^T into
+// Sixteen elementwise warps, four per TMEM lane quadrant, each on 32 of the
+// 128 key columns.  Per step j (key tile j) the MMA thread issues S_{j+1} = Q K_{j+1}^T into
 // the other S buffer before it waits for the elementwise warps' dS_j, so the
 // tensor core computes the next scores while the warps work:
 //   S_{j+1} | wait dS_j: dQ += dS_j K_j, dP_{j+1} = dO V_{j+1}^T | wait dS_{j+1}
 // dP_{j+1} overwrites dS_j only after the MMA that reads it (in-order issue).
 template <int D, bool kCausal>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     tk_attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
@@ -542,14 +549,14 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&sb.v_empty[s], 1);
     }
     mbar_init(&sb.s_full, 1);
-    mbar_init(&sb.p_full, 8);
+    mbar_init(&sb.p_full, 16);
     mbar_init(&sb.acc_full, 1);
-    mbar_init(&sb.acc_empty, 8);
+    mbar_init(&sb.acc_empty, 16);
     mbar_init(&sb.mma_done, 1);
     sb.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 17) {
     tmem_alloc(&sb.tmem_base, 512);
     tmem_relinquish();
   }
@@ -563,9 +570,9 @@ __global__ void __launch_bounds__(320, 1)
   };
   auto s_col = [](uint32_t step) { return (step & 1) ? C::kColS1 : C::kColS; };
 
-  if (warp < 8) {
+  if (warp < 16) {
     // ---------------------------------------------------------- elementwise
-    const int qd = warp & 3, h = warp >> 2;
+    const int qd = warp & 3, h = warp >> 2;  // lane quadrant, column quarter
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
     const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
@@ -588,9 +595,8 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after_sync();
         const uint32_t tS = tmem + lane_off + s_col(it);
         const bool edge = (kCausal && j == i) || (j * 128 + 128 > p.N);
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * h + 32 * c;
+        {
+          const int col0 = 32 * h;
           uint32_t sv[32], dv[32];
           tmem_ld_32x32b_x32(tS + col0, sv);
           tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(320, 1)
                       d0, d1);
             dk[t >> 1] = pack_bf16x2(d0, d1);
           }
-          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
+          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 32 * h, dk);
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -634,8 +640,8 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after_sync();
       const bool valid = qi < p.N;
       __nv_bfloat16 *dst = p.dq + ((size_t)bh * p.N + (valid ? qi : 0)) * D;
-#pragma unroll 1
-      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+      // quarter h of the 128 rows' dQ columns: 32 columns each (D = 64: two quarters)
+      for (int c0 = 32 * h; c0 < D; c0 += 128) {
         uint32_t rv[32];
         tmem_ld_32x32b_x32(tmem + lane_off + C::kColA + c0, rv);
         tmem_wait_ld();
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sb.acc_empty);
     }
-  } else if (warp == 8 && lane == 0) {
+  } else if (warp == 16 && lane == 0) {
     // ---------------------------------------------------------- TMA producer
     uint32_t it = 0, uc = 0;
     bool ok = true;
@@ -700,7 +706,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     for (int i = 0; i < 200 && !ok; ++i) __nanosleep(1000);
-  } else if (warp == 9 && lane == 0) {
+  } else if (warp == 17 && lane == 0) {
     // ---------------------------------------------------------- MMA issue
     constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);
     constexpr uint32_t idG = idesc_f32acc(true, 128, D, false, true);
@@ -752,8 +758,8 @@ __global__ void __launch_bounds__(320, 1)
         }
         tc_fence_after_sync();
         // dQ += dS K (B operand MN-major)
-        issue_grad(tmem + C::kColA, tmem + C::kColdP, sdesc_sw128_lo(k_addr(it), C::kChunkBytes),
-                   dhi, idG, j > 0 ? 1u : 0u);
+        issue_grad<4>(tmem + C::kColA, tmem + C::kColdP,
+                      sdesc_sw128_lo(k_addr(it), C::kChunkBytes), dhi, idG, j > 0 ? 1u : 0u);
         umma_commit(&sb.k_empty[it % KS]);
         if (more) {
           if (!mbar_wait(&sb.v_full[(it + 1) % VS], ((it + 1) / VS) & 1, abort_flag)) {
@@ -777,7 +783,7 @@ __global__ void __launch_bounds__(320, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 17) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
