@@ -43,9 +43,10 @@ if ROOT not in sys.path:
 
 DEFAULT_WORKLOAD = "n1024_d64"
 L2_FLUSH_BYTES = 256 << 20
+# Device code of the forward kernel: recorded DRAM traffic is valid while
+# these files are unchanged.
 KERNEL_SOURCES = ("attention_forward_tk_gb300/csrc/tk_attn_fwd.cuh",
-                  "attention_forward_tk_gb300/csrc/sm103_ptx.cuh",
-                  "attention_forward_tk_gb300/csrc/tk_attn.cu")
+                  "attention_forward_tk_gb300/csrc/sm103_ptx.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_NAME = "tk_attn_fwd_kernel"
 
