@@ -466,3 +466,69 @@ def test_bwd_slices_and_magnitudes(oracle_lib):
         np.testing.assert_array_equal(part[name], full[name][[4, 1]])
     for g in ("dq", "dk", "dv"):
         assert (full["mag_" + g] >= np.abs(full[g]) - 1e-12).all()
+
+
+# --------------------------------------------------------------------------
+# the Based linear-attention oracle
+
+
+def test_based_taylor_values(oracle_lib):
+    from oracle.based import taylor2
+    np.testing.assert_array_equal(taylor2(np.array([0.0, -1.0, 2.0, -2.0, 1.0])),
+                                  [1.0, 0.5, 5.0, 1.0, 2.5])
+    s = np.linspace(-6, 6, 1201)
+    assert taylor2(s).min() == 0.5  # minimum 1/2 at s = -1: the normaliser is never zero
+
+
+def test_based_golden_two_keys(oracle_lib):
+    # Df = 1, scale 1: q1 = 1 against k = (1, -2): T = (2.5, 1) for query 1
+    q = bits([[[[0.0], [1.0]]]])
+    k = bits([[[[1.0], [-2.0]]]])
+    v = bits([[[[2.0, 0.0], [-4.0, 8.0]]]])
+    y, z, _ = oracle_lib.based_quadratic(q, k, v, 1.0, True)
+    np.testing.assert_allclose(z[0, 0], [1.0, 3.5], rtol=1e-15)
+    np.testing.assert_allclose(y[0, 0, 0], [2.0, 0.0], rtol=1e-15)
+    np.testing.assert_allclose(y[0, 0, 1], [(2.5 * 2 - 4) / 3.5, 8 / 3.5], rtol=1e-15)
+
+
+@pytest.mark.parametrize("scale", [0.25, 1.0])
+def test_based_quadratic_equals_recurrent(oracle_lib, scale):
+    # the definition evaluated directly and through explicit 1 + Df + Df^2
+    # feature maps with a running state agree
+    g = torch.Generator().manual_seed(601)
+    q, k = (torch.randn((2, 2, 33, 4), generator=g).to(torch.bfloat16) for _ in range(2))
+    v = torch.randn((2, 2, 33, 5), generator=g).to(torch.bfloat16)
+    y1, z1, _ = oracle_lib.based_quadratic(q, k, v, scale, True)
+    y2, z2 = oracle_lib.based_recurrent(q, k, v, scale)
+    np.testing.assert_allclose(z1, z2, rtol=1e-12)
+    np.testing.assert_allclose(y1, y2, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_based_zero_query_averages(oracle_lib, causal):
+    # q = 0: every T is 1, so y is the (prefix) mean of v and z counts keys
+    g = torch.Generator().manual_seed(611)
+    q = torch.zeros((1, 1, 9, 4), dtype=torch.bfloat16)
+    k = torch.randn((1, 1, 9, 4), generator=g).to(torch.bfloat16)
+    v = torch.randn((1, 1, 9, 3), generator=g).to(torch.bfloat16)
+    y, z, _ = oracle_lib.based_quadratic(q, k, v, 0.5, causal)
+    V = widen(v)[0, 0]
+    if causal:
+        np.testing.assert_allclose(z[0, 0], np.arange(1, 10))
+        np.testing.assert_allclose(y[0, 0], np.cumsum(V, axis=0) / np.arange(1, 10)[:, None],
+                                   rtol=1e-12, atol=1e-15)
+    else:
+        np.testing.assert_allclose(z[0, 0], 9.0)
+        np.testing.assert_allclose(y[0, 0], np.broadcast_to(V.mean(axis=0), (9, 3)), rtol=1e-12,
+                                   atol=1e-15)
+
+
+def test_based_causal_last_row_sees_everything(oracle_lib):
+    g = torch.Generator().manual_seed(621)
+    q, k = (torch.randn((1, 2, 17, 8), generator=g).to(torch.bfloat16) for _ in range(2))
+    v = torch.randn((1, 2, 17, 6), generator=g).to(torch.bfloat16)
+    yc, zc, mc = oracle_lib.based_quadratic(q, k, v, 0.3, True)
+    yn, zn, _ = oracle_lib.based_quadratic(q, k, v, 0.3, False)
+    np.testing.assert_allclose(yc[:, :, -1], yn[:, :, -1], rtol=1e-13)
+    np.testing.assert_allclose(zc[:, :, -1], zn[:, :, -1], rtol=1e-13)
+    assert (mc >= np.abs(yc) - 1e-12).all()
