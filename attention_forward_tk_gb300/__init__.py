@@ -5,8 +5,8 @@ bf16 [B, H, N, D] tensors, computed by hand-written sm_103a CUDA kernels behind
 a C ABI (``include/tk_attn.h``).  This package is the thin Python binding over
 that library: argument marshalling only.  The shared library is loaded on first
 use; if it is missing or cannot be loaded, every call raises.  The library
-also holds the backward pass (dQ, dK, dV) and a bf16 GEMM (C = A B^T) on the
-same TMA / tensor-core pipeline.
+also holds the backward pass (dQ, dK, dV), Based linear attention and a bf16
+GEMM (C = A B^T) on the same TMA / tensor-core pipeline.
 """
 from .api import (  # noqa: F401
     TkAttnError,
@@ -14,6 +14,7 @@ from .api import (  # noqa: F401
     attention_forward,
     attention_forward_host,
     attention_forward_splitkv,
+    based_forward,
     gemm_bf16,
     last_device_error,
     library,
@@ -28,6 +29,8 @@ from .api import (  # noqa: F401
     tk_attn_splitkv_workspace_bytes,
     tk_attn_status_string,
     tk_attn_version,
+    tk_based_check_args,
+    tk_based_fwd,
     tk_gemm_bf16,
     tk_gemm_bf16_check_args,
     version,

@@ -44,6 +44,8 @@ EXPORTED = (
     "tk_attn_bwd",
     "tk_attn_bwd_workspace_bytes",
     "tk_attn_bwd_check_args",
+    "tk_based_fwd",
+    "tk_based_check_args",
 )
 
 
@@ -101,6 +103,10 @@ def library() -> ctypes.CDLL:
         lib.tk_attn_bwd_check_args.restype = i
         lib.tk_attn_bwd_check_args.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
                                                vp, ctypes.c_size_t]
+        lib.tk_based_fwd.restype = i
+        lib.tk_based_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.tk_based_check_args.restype = i
+        lib.tk_based_check_args.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f]
         lib.tk_gemm_bf16.restype = i
         lib.tk_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, vp]
         lib.tk_gemm_bf16_check_args.restype = i
@@ -179,6 +185,18 @@ def tk_attn_bwd_check_args(q: int, k: int, v: int, o: int, lse: int, dout: int, 
     return int(library().tk_attn_bwd_check_args(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D,
                                                  ctypes.c_float(scale), workspace,
                                                  int(workspace_bytes)))
+
+
+def tk_based_fwd(q: int, k: int, v: int, y: int, z: int, B: int, H: int, N: int, Df: int,
+                 Dv: int, scale: float, causal: int, stream: int) -> int:
+    return int(library().tk_based_fwd(q, k, v, y, z, B, H, N, Df, Dv, ctypes.c_float(scale),
+                                      int(causal), stream))
+
+
+def tk_based_check_args(q: int, k: int, v: int, y: int, z: int, B: int, H: int, N: int, Df: int,
+                        Dv: int, scale: float) -> int:
+    return int(library().tk_based_check_args(q, k, v, y, z, B, H, N, Df, Dv,
+                                             ctypes.c_float(scale)))
 
 
 def tk_gemm_bf16(a: int, b: int, c: int, M: int, N: int, K: int, stream: int) -> int:
@@ -304,6 +322,29 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
     if st != TK_ATTN_OK:
         raise TkAttnError(f"tk_attn_bwd: {tk_attn_status_string(st)} ({st})", st)
     return dq, dk, dv
+
+
+def based_forward(q, k, v, causal: bool = True, scale: float | None = None, out=None, z=None,
+                  stream=None):
+    """Based linear attention: y, z for bf16 CUDA tensors q, k [B, H, N, 16] and
+    v [B, H, N, 64] (scale defaults to 1/sqrt(16)).  Enqueued on `stream`."""
+    import torch
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B, H, N, Df] and v [B, H, N, Dv]")
+    B, H, N, Df = (int(x) for x in q.shape)
+    Dv = int(v.shape[3])
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(Df)
+    out = torch.empty_like(v) if out is None else out
+    z = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if z is None else z
+    st = tk_based_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), z.data_ptr(),
+                      B, H, N, Df, Dv, float(scale), int(bool(causal)), _stream_handle(stream))
+    if st != TK_ATTN_OK:
+        raise TkAttnError(f"tk_based_fwd: {tk_attn_status_string(st)} ({st})", st)
+    return out, z
 
 
 def gemm_bf16(a, b, out=None, stream=None):

@@ -20,6 +20,7 @@
 #include "tk_attn_combine.cuh"
 #include "tk_attn_bwd.cuh"
 #include "tk_attn_fwd.cuh"
+#include "tk_based.cuh"
 #include "tk_gemm.cuh"
 
 namespace tkattn {
@@ -101,6 +102,13 @@ void init_device(int dev, DeviceState &ds) {
   if (!st) st = configure_kernel<128, true>();
   if (!st) st = configure_kernel<64, false, true>();
   if (!st) st = configure_kernel<128, false, true>();
+  if (!st && (cudaFuncSetAttribute(tk_based_fwd_kernel<false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   BasedCfg::kSmemAlloc) != cudaSuccess ||
+              cudaFuncSetAttribute(tk_based_fwd_kernel<true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   BasedCfg::kSmemAlloc) != cudaSuccess))
+    st = TK_ATTN_ERR_LAUNCH;
   if (!st) st = configure_bwd<64, false>();
   if (!st) st = configure_bwd<64, true>();
   if (!st) st = configure_bwd<128, false>();
@@ -186,6 +194,22 @@ bool make_map_2d(CUtensorMap *map, const void *ptr, int rows, int K, int box_row
   cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [BH, N, 16] bf16 feature rows (32 bytes each) as a 3-D tensor map: boxes of
+// 16 columns x 128 rows x 1 slice with the 32-byte swizzle; rows past N read
+// as zero.
+bool make_map_feat(CUtensorMap *map, const void *ptr, int BH, int N) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {16, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {32, (cuuint64_t)N * 32};
+  cuuint32_t box[3] = {16, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -625,6 +649,63 @@ extern "C" int tk_attn_bwd(const void *q, const void *k, const void *v, const vo
                : launch_bwd<128, false>(tq, tk, tv, tdo, p, o, dout, lse, lse2, delta,
                                         ds->num_sms, s);
   return e == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------- Based
+
+extern "C" int tk_based_check_args(const void *q, const void *k, const void *v, const void *y,
+                                   const float *z, int B, int H, int N, int Df, int Dv,
+                                   float scale) {
+  if (!q || !k || !v || !y || !z) return TK_ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return TK_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return TK_ATTN_ERR_INVALID_ARG;
+  if (Df != BasedCfg::kDf || Dv != BasedCfg::kDv) return TK_ATTN_ERR_UNSUPPORTED;
+  if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)y | (uintptr_t)z) & 15u)
+    return TK_ATTN_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL || BH * ((N + 127LL) / 128) > 0x7fffffffLL) return TK_ATTN_ERR_UNSUPPORTED;
+  const unsigned long long fb = (unsigned long long)BH * N * Df * 2ull;
+  const unsigned long long vb = (unsigned long long)BH * N * Dv * 2ull;
+  if (vb >= (1ull << 40)) return TK_ATTN_ERR_UNSUPPORTED;
+  const size_t zb = (size_t)BH * N * 4;
+  const uintptr_t py = (uintptr_t)y, pz = (uintptr_t)z;
+  if (overlaps(py, vb, pz, zb) || overlaps(py, vb, (uintptr_t)q, fb) ||
+      overlaps(py, vb, (uintptr_t)k, fb) || overlaps(py, vb, (uintptr_t)v, vb) ||
+      overlaps(pz, zb, (uintptr_t)q, fb) || overlaps(pz, zb, (uintptr_t)k, fb) ||
+      overlaps(pz, zb, (uintptr_t)v, vb))
+    return TK_ATTN_ERR_INVALID_ARG;
+  return TK_ATTN_OK;
+}
+
+extern "C" int tk_based_fwd(const void *q, const void *k, const void *v, void *y, float *z,
+                            int B, int H, int N, int Df, int Dv, float scale, int causal,
+                            tk_attn_stream_t stream) {
+  int st = tk_based_check_args(q, k, v, y, z, B, H, N, Df, Dv, scale);
+  if (st) return st;
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_feat(&tq, q, BH, N) || !make_map_feat(&tk, k, BH, N) ||
+      !make_map(&tv, v, BH, N, Dv))
+    return TK_ATTN_ERR_LAUNCH;
+  BasedParams p;
+  p.y = static_cast<__nv_bfloat16 *>(y);
+  p.z = z;
+  p.err = ds->err_word;
+  p.BH = BH;
+  p.N = N;
+  p.nt = (N + 127) / 128;
+  p.num_units = BH * p.nt;
+  p.scale = scale;
+  const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (causal)
+    tk_based_fwd_kernel<true><<<grid, BasedCfg::kThreads, BasedCfg::kSmemAlloc, s>>>(tq, tk, tv, p);
+  else
+    tk_based_fwd_kernel<false><<<grid, BasedCfg::kThreads, BasedCfg::kSmemAlloc, s>>>(tq, tk, tv,
+                                                                                     p);
+  return cudaGetLastError() == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 
 // ---------------------------------------------------------------- GEMM

@@ -22,6 +22,9 @@ them, split over keys):
 the backward pass (tk_attn_bwd) on the shapes of n4096_d128 and n8192_d128_c,
 with the output gradient dO ~ N(0, 1) drawn after Q, K, V by draw_grad(),
 
+Based linear attention (tk_based_fwd) on B16 H16 N4096, causal, with 16-wide
+feature rows q, k ~ N(0, 1) and 64-wide values v ~ N(0, 1) (draw_based),
+
 and one dense GEMM shape for tk_gemm_bf16 (C = A B^T):
 
   gemm_8192   M = N = K = 8192, A and B ~ N(0, 1)
@@ -148,6 +151,45 @@ def draw_grad(shape, seed: int, device="cpu"):
 
 # The backward pass is measured on the forward's D = 128 shapes.
 BWD_WORKLOADS = tuple(w for w in WORKLOADS if w.name in ("n4096_d128", "n8192_d128_c"))
+
+
+@dataclass(frozen=True)
+class BasedWorkload:
+    name: str
+    B: int
+    H: int
+    N: int
+    causal: bool
+    seed: int
+    Df: int = 16
+    Dv: int = 64
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.Df)
+
+    @property
+    def flops(self) -> float:
+        """Tensor-core FLOPs of the direct (quadratic) evaluation: per visible
+        (query, key) pair 2 Df for the score and 2 Dv for the weighted value,
+        N^2 pairs per slice (halved under the causal mask)."""
+        pairs = self.N * self.N / (2 if self.causal else 1)
+        return self.B * self.H * pairs * 2.0 * (self.Df + self.Dv)
+
+
+BASED_WORKLOADS = (BasedWorkload("based_n4096_c", 16, 16, 4096, True, 8),)
+BASED_BY_NAME = {w.name: w for w in BASED_WORKLOADS}
+
+
+def draw_based(B: int, H: int, N: int, seed: int, Df: int = 16, Dv: int = 64, device="cpu"):
+    """q, k [B, H, N, Df] then v [B, H, N, Dv], N(0, 1) rounded to bf16, from
+    one generator seeded with `seed`."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    q = _randn(g, (B, H, N, Df))
+    k = _randn(g, (B, H, N, Df))
+    v = _randn(g, (B, H, N, Dv))
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
 
 
 @dataclass(frozen=True)

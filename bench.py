@@ -6,6 +6,8 @@
 `--workload bwd_n4096_d128` (or bwd_<any forward workload>) times the backward
 pass, tk_attn_bwd, with the forward's outputs computed beforehand.
 
+`--workload based_n4096_c` times Based linear attention, tk_based_fwd.
+
 `--workload gemm_8192` times the library's bf16 GEMM (tk_gemm_bf16, C = A B^T,
 M = N = K = 8192) instead, with cuBLAS (torch.matmul) on the same operands
 beside it.
@@ -351,6 +353,40 @@ def time_bwd(w, steps: int, warmup: int, device):
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
+def time_based(w, steps: int, warmup: int, device):
+    """CUDA-event times of `steps` tk_based_fwd launches, L2 flushed before each."""
+    import torch
+
+    from attention_forward_tk_gb300 import api
+    from attention_forward_tk_gb300.inputs import draw_based
+
+    q, k, v = draw_based(w.B, w.H, w.N, w.seed, w.Df, w.Dv, device=device)
+    y = torch.empty_like(v)
+    z = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), y.data_ptr(), z.data_ptr(), w.B, w.H, w.N,
+            w.Df, w.Dv, w.scale, int(w.causal), sh)
+    for _ in range(warmup):
+        flush.zero_()
+        st = api.tk_based_fwd(*args)
+        if st:
+            raise RuntimeError(api.tk_attn_status_string(st))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        api.tk_based_fwd(*args)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    if api.tk_attn_last_device_error(sh) != 0:
+        raise RuntimeError("device-side barrier timeout in tk_based_fwd")
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
 def bwd_flops(w) -> float:
     """The backward's five tile products per (query, key) pair against the
     forward's two: 2.5 x the forward FLOPs (the kernels execute seven)."""
@@ -429,11 +465,14 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from attention_forward_tk_gb300.inputs import (BWD_WORKLOADS, BY_NAME, EXTRA_WORKLOADS,
-                                                   GEMM_BY_NAME, GEMM_WORKLOADS, WORKLOADS)
+    from attention_forward_tk_gb300.inputs import (BASED_BY_NAME, BASED_WORKLOADS, BWD_WORKLOADS,
+                                                   BY_NAME, EXTRA_WORKLOADS, GEMM_BY_NAME,
+                                                   GEMM_WORKLOADS, WORKLOADS)
     world, rank, local = dist_env()
     if args.workload in GEMM_BY_NAME:
         return main_gemm(args, GEMM_BY_NAME[args.workload], world, rank, local)
+    if args.workload in BASED_BY_NAME:
+        return main_based(args, BASED_BY_NAME[args.workload], world, rank, local)
     if args.workload.startswith("bwd_") and args.workload[4:] in BY_NAME:
         return main_bwd(args, BY_NAME[args.workload[4:]], world, rank, local)
     w = BY_NAME[args.workload]
@@ -500,6 +539,13 @@ def main():
                                        "tflops": round(bwd_flops(bw) / m / 1e9, 1),
                                        "launches": 60, "sm_mhz": c["sm_mhz"],
                                        "reasons": c["reasons"]}
+        for bw in BASED_WORKLOADS:
+            with ClockSampler(device.index if world == 1 else local) as oclk:
+                bms = time_based(bw, 50, 3, device)
+            m = statistics.median(bms)
+            c = oclk.summary()
+            extra[bw.name] = {"ms": round(m, 4), "tflops": round(bw.flops / m / 1e9, 1),
+                              "launches": 50, "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
         for gw in GEMM_WORKLOADS:
             with ClockSampler(device.index if world == 1 else local) as oclk:
                 gms, cms = time_gemm(gw, 100, 5, device)
@@ -605,6 +651,39 @@ def main_bwd(args, w, world, rank, local):
                      "peak_kind": f"{peak_kind} dense bf16 (burst)", "traffic": None,
                      "executed_tflops": round(1.4 * achieved, 1)},
         "gpu_launches": 3 * args.steps,
+        "kernel_ms_median": round(statistics.median(ms), 5),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main_based(args, w, world, rank, local):
+    """`--workload based_n4096_c`: Based linear attention (tk_based_fwd)."""
+    import torch
+
+    from attention_forward_tk_gb300.build import build_library
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    build_library()
+    with ClockSampler(device.index) as clk:
+        ms = time_based(w, args.steps, args.warmup, device)
+    if rank != 0:
+        return
+    peak_tf, _, peak_kind = measured_peaks()
+    t = statistics.mean(ms)
+    achieved = w.flops / (t / 1e3) / 1e12
+    line = {
+        "metric": "Based linear attention TFLOP/s (bf16, 1xGB300; direct evaluation)",
+        "value": round(achieved, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Df": w.Df, "Dv": w.Dv,
+                   "causal": w.causal, "flops_per_step": w.flops,
+                   "l2": "flushed (256 MB write) before every timed step"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                     "peak_kind": f"{peak_kind} dense bf16 (burst)", "traffic": None},
+        "gpu_launches": args.steps,
         "kernel_ms_median": round(statistics.median(ms), 5),
         "clocks": clk.summary(),
     }

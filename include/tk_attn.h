@@ -61,7 +61,7 @@ typedef struct CUstream_st *tk_attn_stream_t;
 #define TK_ATTN_ERR_TOO_LARGE (-6)      /* tk_attn_fwd_splitkv_static: the ranges'
                                            partial results exceed its static scratch */
 
-#define TK_ATTN_VERSION 10300 /* major*10000 + minor*100 + patch */
+#define TK_ATTN_VERSION 10400 /* major*10000 + minor*100 + patch */
 
 /*
  * tk_attn_fwd -- fused attention forward, asynchronous on `stream`.
@@ -203,6 +203,32 @@ int tk_attn_bwd_check_args(const void *q, const void *k, const void *v, const vo
                            const float *lse, const void *dout, const void *dq, const void *dk,
                            const void *dv, int B, int H, int N, int D, float scale,
                            const void *workspace, size_t workspace_bytes);
+
+/*
+ * tk_based_fwd -- Based linear attention, forward:
+ *
+ *   y_i = sum_{j visible} T(s_ij) v_j / z_i,   z_i = sum_{j visible} T(s_ij),
+ *   s_ij = scale q_i . k_j,   T(s) = 1 + s + s^2 / 2
+ *
+ * (visible: j <= i if causal, else every j).  T is the inner product of the
+ * second-order Taylor feature maps of exp, phi(x) = [1, x, vec(x x^T)/sqrt 2].
+ * The ThunderKittens pages name a Based linear-attention kernel and its
+ * throughput (88811315.cn post 77732; es.news.hada.io topic 14783) without
+ * defining it; this is the published Based form.  T(s) >= 1/2, so z > 0.
+ *
+ *   q, k : bf16 [B, H, N, Df]   feature rows, Df = 16
+ *   v, y : bf16 [B, H, N, Dv]   Dv = 64
+ *   z    : fp32 [B, H, N]       the normaliser
+ *
+ * Same conventions as tk_attn_fwd; scale may be any finite value.  Other
+ * feature or value widths: TK_ATTN_ERR_UNSUPPORTED.
+ */
+int tk_based_fwd(const void *q, const void *k, const void *v, void *y, float *z, int B, int H,
+                 int N, int Df, int Dv, float scale, int causal, tk_attn_stream_t stream);
+
+/* The argument checks of tk_based_fwd alone (no GPU needed). */
+int tk_based_check_args(const void *q, const void *k, const void *v, const void *y,
+                        const float *z, int B, int H, int N, int Df, int Dv, float scale);
 
 /*
  * tk_gemm_bf16 -- dense bf16 matrix product with fp32 accumulation:

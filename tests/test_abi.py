@@ -14,7 +14,7 @@ HEADER = os.path.join(ROOT, "include", "tk_attn.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(tk_(?:attn|gemm)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(tk_(?:attn|gemm|based)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_names(tk_lib):
@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol(tk_lib):
 
 
 def test_version_and_status_strings(tk_lib):
-    assert tk_lib.tk_attn_version() == 10300
+    assert tk_lib.tk_attn_version() == 10400
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = tk_lib.tk_attn_status_string(code)
         assert s and s != "unknown status"
