@@ -15,7 +15,8 @@
 // running maximum, since T > 0 needs no stabilising shift.  One unit = (slice,
 // 128-query tile); K/V tiles stream through a ring.  Per key tile:
 //   S = Q K^T       one M128 N128 K16 MMA (32-byte-swizzled 16-wide rows)
-//   A = T(scale S)  eight elementwise warps, bf16 into S's TMEM columns
+//   A = T(scale S)  sixteen elementwise warps (four per TMEM lane quadrant,
+//                   32 key columns each), bf16 into S's TMEM columns
 //   O += A V        TS MMAs (A from TMEM, V MN-major)
 // S has two TMEM buffers, so the next tile's S runs while the warps work.
 #pragma once
@@ -39,7 +40,7 @@ struct BasedCfg {
   static constexpr int kStageBytes = kQKBytes + kVBytes;
   static constexpr int kStages = 8;
   static constexpr int kSmemAlloc = kQKBytes + kStages * kStageBytes + 1024;
-  static constexpr int kThreads = 320;  // 8 elementwise warps, producer, MMA
+  static constexpr int kThreads = 576;  // 16 elementwise warps, producer, MMA
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 };
 
@@ -47,13 +48,13 @@ struct BasedShared {
   uint64_t fix_full, fix_empty;  // the unit's Q tile landed / released
   uint64_t kv_full[BasedCfg::kStages], kv_empty[BasedCfg::kStages];
   uint64_t s_full[2];            // S into buffer b complete       (commit)
-  uint64_t p_full[2];            // bf16 A in buffer b             (8 warps)
-  uint64_t lsum_bar;             // partial row sums written       (8 warps)
-  uint64_t acc_full, acc_empty;  // O of a unit done / read        (commit / 8 warps)
+  uint64_t p_full[2];            // bf16 A in buffer b             (16 warps)
+  uint64_t lsum_bar;             // partial row sums written       (16 warps)
+  uint64_t acc_full, acc_empty;  // O of a unit done / read        (commit / 16 warps)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float lsum[2][2][128];         // [unit parity][column half][row] partial row sums
+  float lsum[2][4][128];         // [unit parity][column quarter][row] partial row sums
 };
 
 // Shared-memory descriptor, K-major, 32-byte swizzle: 8-row groups of 32-byte
@@ -79,7 +80,7 @@ __device__ __forceinline__ void based_unit(const BasedParams &p, int u, int &bh,
 }
 
 template <bool kCausal>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     tk_based_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const BasedParams p) {
@@ -101,16 +102,16 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(&sb.s_full[0], 1);
     mbar_init(&sb.s_full[1], 1);
-    mbar_init(&sb.p_full[0], 8);
-    mbar_init(&sb.p_full[1], 8);
-    mbar_init(&sb.lsum_bar, 8);
+    mbar_init(&sb.p_full[0], 16);
+    mbar_init(&sb.p_full[1], 16);
+    mbar_init(&sb.lsum_bar, 16);
     mbar_init(&sb.acc_full, 1);
-    mbar_init(&sb.acc_empty, 8);
+    mbar_init(&sb.acc_empty, 16);
     mbar_init(&sb.mma_done, 1);
     sb.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 17) {
     tmem_alloc(&sb.tmem_base, 512);
     tmem_relinquish();
   }
@@ -128,9 +129,9 @@ __global__ void __launch_bounds__(320, 1)
   // waiter (a parity wait cannot tell phase t from phase t + 2).
   auto s_col = [](uint32_t step) { return (step & 1) ? C::kColS1 : C::kColS0; };
 
-  if (warp < 8) {
+  if (warp < 16) {
     // ---------------------------------------------------------- elementwise
-    const int qd = warp & 3, h = warp >> 2;  // lane quadrant, column half
+    const int qd = warp & 3, h = warp >> 2;  // lane quadrant, column quarter
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
     const uint64_t sc2 = f2_pack(p.scale, p.scale);
@@ -153,9 +154,8 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after_sync();
         const uint32_t tS = tmem + lane_off + s_col(it);
         const bool edge = (kCausal && j == i) || (j * 128 + 128 > p.N);
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * h + 32 * c;
+        {
+          const int col0 = 32 * h;
           uint32_t sv[32];
           tmem_ld_32x32b_x32(tS + col0, sv);
           tmem_wait_ld();
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(320, 1)
             pk[t >> 1] = pack_bf16x2(a0, a1);
             pk[(t >> 1) + 1] = pack_bf16x2(a2, a3);
           }
-          tmem_st_32x32b_x16(tS + 64 * h + 16 * c, pk);
+          tmem_st_32x32b_x16(tS + 32 * h, pk);
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -203,36 +203,36 @@ __global__ void __launch_bounds__(320, 1)
         fail();
         break;
       }
-      const float l = sb.lsum[uc & 1][0][r] + sb.lsum[uc & 1][1][r];
+      const float l = (sb.lsum[uc & 1][0][r] + sb.lsum[uc & 1][1][r]) +
+                      (sb.lsum[uc & 1][2][r] + sb.lsum[uc & 1][3][r]);
       if (!mbar_wait(&sb.acc_full, uc & 1, abort_flag)) {
         fail();
         break;
       }
       tc_fence_after_sync();
-      uint32_t rv[32];
-      tmem_ld_32x32b_x32(tmem + lane_off + C::kColO + 32 * h, rv);
+      // quarter h of the 64 output columns: 16 each
+      uint32_t rv[16];
+      tmem_ld_32x32b_x16(tmem + lane_off + C::kColO + 16 * h, rv);
       tmem_wait_ld();
       const float inv = 1.f / l;
-      uint32_t pk[16];
+      uint32_t pk[8];
 #pragma unroll
-      for (int t = 0; t < 32; t += 2) {
+      for (int t = 0; t < 16; t += 2) {
         reg_barrier(rv[t]);
         reg_barrier(rv[t + 1]);
         pk[t >> 1] = pack_bf16x2(__uint_as_float(rv[t]) * inv, __uint_as_float(rv[t + 1]) * inv);
       }
       if (qi < p.N) {
-        __nv_bfloat16 *dst = p.y + ((size_t)bh * p.N + qi) * C::kDv + 32 * h;
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          *reinterpret_cast<uint4 *>(dst + 8 * t) =
-              make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        __nv_bfloat16 *dst = p.y + ((size_t)bh * p.N + qi) * C::kDv + 16 * h;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         if (h == 0) p.z[(size_t)bh * p.N + qi] = l;
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sb.acc_empty);
     }
-  } else if (warp == 8 && lane == 0) {
+  } else if (warp == 16 && lane == 0) {
     // ---------------------------------------------------------- TMA producer
     uint32_t it = 0, uc = 0;
     bool ok = true;
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     for (int i = 0; i < 200 && !ok; ++i) __nanosleep(1000);
-  } else if (warp == 9 && lane == 0) {
+  } else if (warp == 17 && lane == 0) {
     // ---------------------------------------------------------- MMA issue
     constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);
     constexpr uint32_t idO = idesc_f32acc(true, 128, C::kDv, false, true);
@@ -299,8 +299,8 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after_sync();
-        // O += A V (A from TMEM in two column halves, V MN-major)
-        issue_grad<2>(tmem + C::kColO, tmem + s_col(it),
+        // O += A V (A from TMEM in four column quarters, V MN-major)
+        issue_grad<4>(tmem + C::kColO, tmem + s_col(it),
                       sdesc_sw128_lo(k_addr(it) + C::kQKBytes, 16384), dhi, idO, j > 0 ? 1u : 0u);
         umma_commit(&sb.kv_empty[it % S]);
         if (j + 2 < n) {
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(320, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 17) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
