@@ -698,6 +698,12 @@ extern "C" int tk_based_fwd(const void *q, const void *k, const void *v, void *y
   p.nt = (N + 127) / 128;
   p.num_units = BH * p.nt;
   p.scale = scale;
+  {  // causal sections: K and V of a slice take N * (16 + 64) * 2 bytes; ~64 MB per section
+    long long g = (64LL << 20) / ((long long)N * (BasedCfg::kDf + BasedCfg::kDv) * 2);
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    p.head_group = (int)g;
+  }
   const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (causal)

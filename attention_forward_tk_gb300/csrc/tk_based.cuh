@@ -30,6 +30,7 @@ struct BasedParams {
   float *z;          // [BH, N] normaliser
   int *err;
   int BH, N, nt, num_units;
+  int head_group;  // causal order: slices per L2-sized section
   float scale;
 };
 
@@ -65,12 +66,19 @@ __device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr) {
          (1ull << 46) | (6ull << 61);
 }
 
+// Causal: slices in sections of head_group whose K and V fit in about half
+// the L2, longest query tiles first within a section (tile i meets i + 1 key
+// tiles), so the CTAs running at one time share K/V out of L2.
 template <bool kCausal>
 __device__ __forceinline__ void based_unit(const BasedParams &p, int u, int &bh, int &i, int &n) {
-  if (kCausal) {  // longest first: query tile i meets i + 1 key tiles
-    const int r = u / p.BH;
-    bh = u - r * p.BH;
-    i = p.nt - 1 - r;
+  if (kCausal) {
+    const int per = p.head_group * p.nt;
+    const int g = u / per;
+    const int r = u - g * per;
+    const int hg = min(p.head_group, p.BH - g * p.head_group);
+    const int t = r / hg;
+    bh = g * p.head_group + (r - t * hg);
+    i = p.nt - 1 - t;
     n = i + 1;
   } else {
     bh = u / p.nt;
@@ -134,8 +142,10 @@ __global__ void __launch_bounds__(576, 1)
     const int qd = warp & 3, h = warp >> 2;  // lane quadrant, column quarter
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
-    const uint64_t sc2 = f2_pack(p.scale, p.scale);
-    const uint64_t hsc2 = f2_pack(0.5f * p.scale, 0.5f * p.scale);
+    // T(scale x) = 1 + x (c + x c^2 / 2), c = scale: two packed FMAs per pair
+    const uint64_t c2 = f2_pack(p.scale, p.scale);
+    const float hc = 0.5f * p.scale * p.scale;
+    const uint64_t hcc2 = f2_pack(hc, hc);
     const uint64_t one2 = f2_pack(1.f, 1.f);
     uint32_t it = 0, uc = 0;
     bool ok = true;
@@ -166,21 +176,27 @@ __global__ void __launch_bounds__(576, 1)
             reg_barrier(sv[t + 1]);
             reg_barrier(sv[t + 2]);
             reg_barrier(sv[t + 3]);
-            // T(s) = 1 + s (1 + s / 2), s = scale * S
             const uint64_t x0 = f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
             const uint64_t x1 = f2_pack(__uint_as_float(sv[t + 2]), __uint_as_float(sv[t + 3]));
-            float a0, a1, a2, a3;
-            f2_unpack(f2_fma(f2_mul(x0, sc2), f2_fma(x0, hsc2, one2), one2), a0, a1);
-            f2_unpack(f2_fma(f2_mul(x1, sc2), f2_fma(x1, hsc2, one2), one2), a2, a3);
-            if (edge) {
+            uint64_t t0 = f2_fma(x0, f2_fma(x0, hcc2, c2), one2);
+            uint64_t t1 = f2_fma(x1, f2_fma(x1, hcc2, c2), one2);
+            if (edge) {  // the diagonal tile or a ragged tail only
+              float a0, a1, a2, a3;
+              f2_unpack(t0, a0, a1);
+              f2_unpack(t1, a2, a3);
               const int kj = j * 128 + col0 + t;
               if ((kCausal && kj > qi) || kj >= p.N) a0 = 0.f;
               if ((kCausal && kj + 1 > qi) || kj + 1 >= p.N) a1 = 0.f;
               if ((kCausal && kj + 2 > qi) || kj + 2 >= p.N) a2 = 0.f;
               if ((kCausal && kj + 3 > qi) || kj + 3 >= p.N) a3 = 0.f;
+              t0 = f2_pack(a0, a1);
+              t1 = f2_pack(a2, a3);
             }
-            la = f2_add(la, f2_pack(a0, a1));
-            lb = f2_add(lb, f2_pack(a2, a3));
+            la = f2_add(la, t0);
+            lb = f2_add(lb, t1);
+            float a0, a1, a2, a3;
+            f2_unpack(t0, a0, a1);
+            f2_unpack(t1, a2, a3);
             pk[t >> 1] = pack_bf16x2(a0, a1);
             pk[(t >> 1) + 1] = pack_bf16x2(a2, a3);
           }
