@@ -18,7 +18,7 @@
 //   A = T(scale S)  sixteen elementwise warps (four per TMEM lane quadrant,
 //                   32 key columns each), bf16 into S's TMEM columns
 //   O += A V        TS MMAs (A from TMEM, V MN-major)
-// S has two TMEM buffers, so the next tile's S runs while the warps work.
+// S has three TMEM buffers, so the next tiles' S run while the warps work.
 #pragma once
 
 #include "tk_attn_bwd.cuh"
@@ -42,14 +42,15 @@ struct BasedCfg {
   static constexpr int kStages = 8;
   static constexpr int kSmemAlloc = kQKBytes + kStages * kStageBytes + 1024;
   static constexpr int kThreads = 576;  // 16 elementwise warps, producer, MMA
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr int kSBufs = 3;  // S buffers in TMEM, 128 columns each
+  static constexpr uint32_t kColO = 128 * kSBufs;
 };
 
 struct BasedShared {
   uint64_t fix_full, fix_empty;  // the unit's Q tile landed / released
   uint64_t kv_full[BasedCfg::kStages], kv_empty[BasedCfg::kStages];
-  uint64_t s_full[2];            // S into buffer b complete       (commit)
-  uint64_t p_full[2];            // bf16 A in buffer b             (16 warps)
+  uint64_t s_full[BasedCfg::kSBufs];  // S into buffer b complete  (commit)
+  uint64_t p_full[BasedCfg::kSBufs];  // bf16 A in buffer b        (16 warps)
   uint64_t lsum_bar;             // partial row sums written       (16 warps)
   uint64_t acc_full, acc_empty;  // O of a unit done / read        (commit / 16 warps)
   uint64_t mma_done;
@@ -108,10 +109,10 @@ __global__ void __launch_bounds__(576, 1)
       mbar_init(&sb.kv_full[s], 1);
       mbar_init(&sb.kv_empty[s], 1);
     }
-    mbar_init(&sb.s_full[0], 1);
-    mbar_init(&sb.s_full[1], 1);
-    mbar_init(&sb.p_full[0], 16);
-    mbar_init(&sb.p_full[1], 16);
+    for (int b = 0; b < C::kSBufs; ++b) {
+      mbar_init(&sb.s_full[b], 1);
+      mbar_init(&sb.p_full[b], 16);
+    }
     mbar_init(&sb.lsum_bar, 16);
     mbar_init(&sb.acc_full, 1);
     mbar_init(&sb.acc_empty, 16);
@@ -131,11 +132,12 @@ __global__ void __launch_bounds__(576, 1)
     sb.abort = 1;
     atomicCAS(p.err, 0, kDevErrTimeout);
   };
-  // Step t uses S buffer t & 1, with its own s_full and p_full barriers: the
-  // next step's S is already in flight when a step's A is published, so one
+  // Step t uses S buffer t % 3, with its own s_full and p_full barriers: the
+  // next steps' S are already in flight when a step's A is published, so one
   // barrier per buffer keeps every barrier at most one phase ahead of its
   // waiter (a parity wait cannot tell phase t from phase t + 2).
-  auto s_col = [](uint32_t step) { return (step & 1) ? C::kColS1 : C::kColS0; };
+  constexpr uint32_t NB = C::kSBufs;
+  auto s_col = [](uint32_t step) { return 128u * (step % NB); };
 
   if (warp < 16) {
     // ---------------------------------------------------------- elementwise
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(576, 1)
       uint64_t la = f2_pack(0.f, 0.f), lb = la;
 #pragma unroll 1
       for (int j = 0; j < n; ++j, ++it) {
-        if (!mbar_wait(&sb.s_full[it & 1], (it >> 1) & 1, abort_flag)) {
+        if (!mbar_wait(&sb.s_full[it % NB], (it / NB) & 1, abort_flag)) {
           fail();
           ok = false;
           break;
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(576, 1)
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sb.p_full[it & 1]);
+        if (lane == 0) mbar_arrive(&sb.p_full[it % NB]);
       }
       if (!ok) break;
       // ---- epilogue: y = O / z for this query tile (rows < N), z
@@ -287,12 +289,12 @@ __global__ void __launch_bounds__(576, 1)
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
       int bh, i, n;
       based_unit<kCausal>(p, u, bh, i, n);
-      // S of the first two steps, one per buffer
+      // S of the first steps, one per buffer
       if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag)) {
         fail();
         break;
       }
-      for (int j = 0; j < 2 && j < n && ok; ++j) {
+      for (int j = 0; j < (int)NB && j < n && ok; ++j) {
         if (!mbar_wait(&sb.kv_full[(it + j) % S], ((it + j) / S) & 1, abort_flag)) {
           fail();
           ok = false;
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(576, 1)
         }
         tc_fence_after_sync();
         umma_bf16_ss(tmem + s_col(it + j), qdesc, sdesc_sw32(k_addr(it + j)), idS, 0);
-        umma_commit(&sb.s_full[(it + j) & 1]);
+        umma_commit(&sb.s_full[(it + j) % NB]);
         if (j == n - 1) umma_commit(&sb.fix_empty);  // Q is read by the S products only
       }
       if (!ok) break;
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(576, 1)
         break;
       }
       for (int j = 0; j < n; ++j, ++it) {
-        if (!mbar_wait(&sb.p_full[it & 1], (it >> 1) & 1, abort_flag)) {
+        if (!mbar_wait(&sb.p_full[it % NB], (it / NB) & 1, abort_flag)) {
           fail();
           ok = false;
           break;
@@ -319,17 +321,17 @@ __global__ void __launch_bounds__(576, 1)
         issue_grad<4>(tmem + C::kColO, tmem + s_col(it),
                       sdesc_sw128_lo(k_addr(it) + C::kQKBytes, 16384), dhi, idO, j > 0 ? 1u : 0u);
         umma_commit(&sb.kv_empty[it % S]);
-        if (j + 2 < n) {
-          // S two steps ahead, into the buffer this step's A has just left
-          if (!mbar_wait(&sb.kv_full[(it + 2) % S], ((it + 2) / S) & 1, abort_flag)) {
+        if (j + (int)NB < n) {
+          // S three steps ahead, into the buffer this step's A has just left
+          if (!mbar_wait(&sb.kv_full[(it + NB) % S], ((it + NB) / S) & 1, abort_flag)) {
             fail();
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          umma_bf16_ss(tmem + s_col(it + 2), qdesc, sdesc_sw32(k_addr(it + 2)), idS, 0);
-          umma_commit(&sb.s_full[(it + 2) & 1]);
-          if (j + 3 == n) umma_commit(&sb.fix_empty);
+          umma_bf16_ss(tmem + s_col(it + NB), qdesc, sdesc_sw32(k_addr(it + NB)), idS, 0);
+          umma_commit(&sb.s_full[(it + NB) % NB]);
+          if (j + (int)NB + 1 == n) umma_commit(&sb.fix_empty);
         }
       }
       if (!ok) break;
