@@ -368,14 +368,32 @@ def gemm_bf16(a, b, out=None, stream=None):
     return out
 
 
+_copy_streams = {}
+
+
+def _side_streams(device):
+    """Two streams per device for the host-buffer call's copies, made once."""
+    import torch
+    key = device.index
+    if key not in _copy_streams:
+        _copy_streams[key] = (torch.cuda.Stream(device), torch.cuda.Stream(device))
+    return _copy_streams[key]
+
+
 def attention_forward_host(q, k, v, causal: bool = False, scale: float | None = None,
-                           device_buffers=None, out=None, lse=None, stream=None):
+                           device_buffers=None, out=None, lse=None, stream=None,
+                           chunks: int = 4):
     """The same call for bf16 tensors in (preferably pinned) host memory.
 
     Copies q, k, v to the device, runs tk_attn_fwd, copies O and LSE back into
     host tensors `out` / `lse` (allocated pinned when not given) and waits for
-    the stream.  `device_buffers` = (q_d, k_d, v_d, o_d, lse_d) reuses device
-    memory between calls.  Returns (out, lse) on the host.
+    the work to finish.  `device_buffers` = (q_d, k_d, v_d, o_d, lse_d) reuses
+    device memory between calls.  Returns (out, lse) on the host.
+
+    The batch is cut into `chunks` pieces (batch entries are independent
+    problems), pipelined over three streams: the host-to-device copies of
+    piece c + 1 and the device-to-host copies of piece c - 1 overlap the
+    kernel on piece c, which runs on `stream` (default: the current stream).
     """
     import torch
     B, H, N, D = (int(x) for x in q.shape)
@@ -390,12 +408,23 @@ def attention_forward_host(q, k, v, causal: bool = False, scale: float | None = 
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
     s = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(s):
-        qd.copy_(q, non_blocking=True)
-        kd.copy_(k, non_blocking=True)
-        vd.copy_(v, non_blocking=True)
-        attention_forward(qd, kd, vd, causal, scale, out=od, lse=ld, stream=s)
-        out.copy_(od, non_blocking=True)
-        lse.copy_(ld, non_blocking=True)
+    s_in, s_out = _side_streams(dev)
+    pieces = max(1, min(int(chunks), B))
+    bounds = [B * c // pieces for c in range(pieces + 1)]
+    s_in.wait_stream(s)
+    for c in range(pieces):
+        sl = slice(bounds[c], bounds[c + 1])
+        with torch.cuda.stream(s_in):
+            qd[sl].copy_(q[sl], non_blocking=True)
+            kd[sl].copy_(k[sl], non_blocking=True)
+            vd[sl].copy_(v[sl], non_blocking=True)
+        s.wait_stream(s_in)
+        attention_forward(qd[sl], kd[sl], vd[sl], causal, scale, out=od[sl], lse=ld[sl],
+                          stream=s)
+        s_out.wait_stream(s)
+        with torch.cuda.stream(s_out):
+            out[sl].copy_(od[sl], non_blocking=True)
+            lse[sl].copy_(ld[sl], non_blocking=True)
+    s.wait_stream(s_out)
     s.synchronize()
     return out, lse

@@ -152,3 +152,14 @@ def test_host_buffer_path_matches(tk_lib, oracle_lib):
     o, lse = attention_forward_host(q, k, v, causal=False)
     o_ref, lse_ref = oracle_lib.attention(q, k, v, 0.125, False)
     compare(o.float().double().numpy(), lse.double().numpy(), o_ref, lse_ref, "host path")
+
+
+def test_host_buffer_pieces_match_one_piece(tk_lib):
+    # the pipelined pieces of the batch give exactly the single-call result
+    from attention_forward_tk_gb300 import attention_forward_host
+    q, k, v = draw((5, 2, 384, 128), seed=10)
+    q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    o1, l1 = attention_forward_host(q, k, v, causal=True, chunks=1)
+    o1, l1 = o1.clone(), l1.clone()
+    o4, l4 = attention_forward_host(q, k, v, causal=True, chunks=4)
+    assert torch.equal(o1, o4) and torch.equal(l1, l4)
