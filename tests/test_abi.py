@@ -141,3 +141,48 @@ def test_gemm_rejects_bad_arguments_before_touching_cuda(tk_lib):
     assert chk(b=A, N=256) == tk_lib.TK_ATTN_OK
     # the full call checks first, so it needs no GPU to reject
     assert tk_lib.tk_gemm_bf16(A, B_, C, 256, 500, 128, 0) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_rejects_bad_arguments_before_touching_cuda(tk_lib):
+    DO, DQ, DK, DV, WS = (6 << 40), (7 << 40), (8 << 40), (9 << 40), (10 << 40)
+    need = tk_lib.tk_attn_bwd_workspace_bytes(2, 3, 100, 64)
+    assert need == 2 * 6 * 128 * 4  # two fp32 rows per padded 128-row tile
+    assert tk_lib.tk_attn_bwd_workspace_bytes(2, 3, 100, 96) == 0
+
+    def chk(q=Q, k=K, v=V, o=O, lse=L, do=DO, dq=DQ, dk=DK, dv=DV, B=2, H=3, N=100, D=64,
+            scale=0.125, ws=WS, wsb=need):
+        return tk_lib.tk_attn_bwd_check_args(q, k, v, o, lse, do, dq, dk, dv, B, H, N, D, scale,
+                                             ws, wsb)
+    assert chk() == tk_lib.TK_ATTN_OK
+    assert chk(do=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(ws=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(N=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(scale=float("nan")) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(wsb=need - 4) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(D=96) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    assert chk(dk=DK + 8) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    # dq inside q, dv inside dk, the workspace inside dv
+    assert chk(dq=Q + 64) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(dv=DK + 64) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(ws=DV + 64) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    # the full call checks first, so it needs no GPU to reject
+    assert tk_lib.tk_attn_bwd(Q, K, V, O, L, DO, DQ, DK, DV, 2, 3, 100, 96, 0.125, 0, WS, need,
+                              0) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+
+
+def test_based_rejects_bad_arguments_before_touching_cuda(tk_lib):
+    def chk(q=Q, k=K, v=V, y=O, z=L, B=2, H=3, N=100, Df=16, Dv=64, scale=0.25):
+        return tk_lib.tk_based_check_args(q, k, v, y, z, B, H, N, Df, Dv, scale)
+    assert chk() == tk_lib.TK_ATTN_OK
+    assert chk(scale=-0.5) == tk_lib.TK_ATTN_OK  # T(s) >= 1/2 for any real s
+    assert chk(scale=float("inf")) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(v=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(H=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(Df=32) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    assert chk(Dv=128) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    assert chk(z=L + 4) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    # y [2,3,100,64] bf16 = 76800 bytes: z inside it, or y over v
+    assert chk(z=O + 1024) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert chk(y=V + 512) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert tk_lib.tk_based_fwd(Q, K, V, O, L, 2, 3, 100, 32, 64, 0.25, 1, 0) == \
+        tk_lib.TK_ATTN_ERR_UNSUPPORTED
