@@ -96,3 +96,30 @@ def test_bench_rejects_too_few_warmups():
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"]
     res = subprocess.run(cmd, capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert res.returncode != 0
+
+
+def test_flop_counts_of_the_other_workloads():
+    from attention_forward_tk_gb300.inputs import (BASED_BY_NAME, BWD_WORKLOADS, BY_NAME,
+                                                   GEMM_BY_NAME)
+    w = BY_NAME["n4096_d128"]
+    assert bench.bwd_flops(w) == 2.5 * 4 * 16 * 16 * 4096 ** 2 * 128
+    assert [x.name for x in BWD_WORKLOADS] == ["n4096_d128", "n8192_d128_c"]
+    b = BASED_BY_NAME["based_n4096_c"]
+    assert b.flops == 16 * 16 * (4096 ** 2 / 2) * 2 * (16 + 64)
+    g = GEMM_BY_NAME["gemm_8192"]
+    assert g.flops == 2 * 8192 ** 3
+    assert g.io_bytes == 3 * 8192 * 8192 * 2
+
+
+def test_input_generators_are_seeded():
+    import torch
+    from attention_forward_tk_gb300.inputs import draw_based, draw_gemm, draw_grad
+    a1, b1 = draw_gemm(16, 24, 32, 3)
+    a2, b2 = draw_gemm(16, 24, 32, 3)
+    assert torch.equal(a1, a2) and torch.equal(b1, b2) and not torch.equal(a1[:, :24], b1[:16])
+    q1, k1, v1 = draw_based(1, 2, 40, 5)
+    q2, k2, v2 = draw_based(1, 2, 40, 5)
+    assert torch.equal(q1, q2) and torch.equal(v1, v2) and q1.shape[-1] == 16 and v1.shape[-1] == 64
+    g1 = draw_grad((1, 1, 8, 64), 2)
+    assert torch.equal(g1, draw_grad((1, 1, 8, 64), 2))
+    assert not torch.equal(g1, draw_grad((1, 1, 8, 64), 3))
