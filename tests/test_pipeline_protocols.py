@@ -1,4 +1,4 @@
-"""Barrier protocols of the backward and Based kernels, checked on the CPU.
+"""Barrier protocols of the backward, Based and GEMM kernels, checked on the CPU.
 
 Each kernel role (TMA producer, MMA issuer, elementwise warps) is replayed
 as the sequence of mbarrier operations its source performs, in the same
@@ -275,6 +275,74 @@ def dkdv_roles(sim, units, S=2):
             yield ("arrive", "acc_empty")
 
     return {"producer": producer(), "mma": mma(), "warps": warps()}
+
+
+def gemm_pair_roles(sim, tiles, k_blocks, S=6):
+    """tk_gemm_kernel, one CTA pair: both CTAs' producers, the first CTA's MMA
+    thread, both CTAs' epilogues and TMEM-release waits.  `full` lives in the
+    first CTA and completes on that CTA's expect-tx arrival plus both CTAs'
+    copies; MMA commits multicast to both CTAs' barriers."""
+    for s_ in range(S):
+        sim.bar(f"full{s_}", 3)
+        for r in range(2):
+            sim.bar(f"empty{r}_{s_}")
+    for b in range(2):
+        sim.bar(f"acc_empty{b}", 2)
+        for r in range(2):
+            sim.bar(f"acc_full{r}_{b}")
+    for r in range(2):
+        sim.bar(f"mma_done{r}")
+
+    def producer(r):
+        it = 0
+        for _ in range(tiles):
+            for _ in range(k_blocks):
+                s_ = it % S
+                if it >= S:
+                    yield ("wait", f"empty{r}_{s_}", it // S - 1)
+                if r == 0:
+                    yield ("arrive", f"full{s_}")
+                yield ("commit", f"full{s_}", f"tma{r}")
+                it += 1
+        for s_ in range(min(S, it)):  # the last commits on this CTA's stages
+            last = it - 1 - ((it - 1 - s_) % S)
+            yield ("wait", f"empty{r}_{s_}", last // S)
+
+    def mma():
+        it = 0
+        for tc in range(tiles):
+            b = tc & 1
+            if tc >= 2:
+                yield ("wait", f"acc_empty{b}", (tc >> 1) - 1)
+            for _ in range(k_blocks):
+                yield ("wait", f"full{it % S}", it // S)
+                yield ("commit", f"empty0_{it % S}")
+                yield ("commit", f"empty1_{it % S}")
+                it += 1
+            yield ("commit", f"acc_full0_{b}")
+            yield ("commit", f"acc_full1_{b}")
+        for i in range(max(0, tiles - 2), tiles):
+            yield ("wait", f"acc_empty{i & 1}", i >> 1)
+        yield ("commit", "mma_done0")
+        yield ("commit", "mma_done1")
+
+    def epilogue(r):
+        for tc in range(tiles):
+            yield ("wait", f"acc_full{r}_{tc & 1}", tc >> 1)
+            yield ("arrive", f"acc_empty{tc & 1}")
+
+    def release(r):
+        yield ("wait", f"mma_done{r}", 0)
+
+    return {"prod0": producer(0), "prod1": producer(1), "mma": mma(), "epi0": epilogue(0),
+            "epi1": epilogue(1), "rel0": release(0), "rel1": release(1)}
+
+
+@pytest.mark.parametrize("tiles,k_blocks", [(1, 1), (1, 7), (2, 3), (3, 1), (5, 4), (4, 13)])
+def test_gemm_pair_protocol(tiles, k_blocks):
+    for seed in range(60):
+        sim = Sim(seed)
+        sim.run(gemm_pair_roles(sim, tiles, k_blocks))
 
 
 UNIT_LISTS = [[1], [2], [3], [4], [1, 1, 1], [5, 1, 2, 7], [3, 3], [1, 4, 1, 9, 2]]
