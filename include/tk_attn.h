@@ -1,6 +1,12 @@
 /*
  * tk_attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
  *
+ * Entry points: tk_attn_fwd (the forward pass, below), tk_attn_fwd_splitkv
+ * and tk_attn_fwd_splitkv_static (queries against a longer key set, keys
+ * split into ranges), tk_attn_bwd (dQ, dK, dV), tk_based_fwd (Based linear
+ * attention) and tk_gemm_bf16 (C = A B^T), each with argument checks that
+ * need no GPU, plus status, version and device-error queries.
+ *
  * The operation (one call = one whole forward pass over B*H independent
  * (batch, head) slices):
  *
