@@ -469,6 +469,8 @@ def main():
                                                    BY_NAME, EXTRA_WORKLOADS, GEMM_BY_NAME,
                                                    GEMM_WORKLOADS, WORKLOADS)
     world, rank, local = dist_env()
+    if args.impl == "reference" and args.workload not in BY_NAME:
+        ap.error("--impl reference times the oracle on the attention forward workloads only")
     if args.workload in GEMM_BY_NAME:
         return main_gemm(args, GEMM_BY_NAME[args.workload], world, rank, local)
     if args.workload in BASED_BY_NAME:
