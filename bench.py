@@ -469,6 +469,10 @@ def main():
                                                    BY_NAME, EXTRA_WORKLOADS, GEMM_BY_NAME,
                                                    GEMM_WORKLOADS, WORKLOADS)
     world, rank, local = dist_env()
+    known = (set(BY_NAME) | set(GEMM_BY_NAME) | set(BASED_BY_NAME) |
+             {"bwd_" + n for n in BY_NAME})
+    if args.workload not in known:
+        ap.error(f"unknown workload {args.workload!r}; one of {', '.join(sorted(known))}")
     if args.impl == "reference" and args.workload not in BY_NAME:
         ap.error("--impl reference times the oracle on the attention forward workloads only")
     if args.workload in GEMM_BY_NAME:
