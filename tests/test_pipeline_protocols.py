@@ -1,4 +1,4 @@
-"""Barrier protocols of the backward, Based and GEMM kernels, checked on the CPU.
+"""Barrier protocols of the forward, backward, Based and GEMM kernels, checked on the CPU.
 
 Each kernel role (TMA producer, MMA issuer, elementwise warps) is replayed
 as the sequence of mbarrier operations its source performs, in the same
@@ -9,6 +9,12 @@ order, under many random interleavings and completion delays:
   commit(bar)    asynchronous arrival when everything issued before it has
                  finished: tensor-core commits and TMA completions land later,
                  in issue order per issuing thread
+  check(bar, k)  a use of data that phase k of `bar` guards, without a wait of
+                 its own (the role relies on another role's wait): phase k
+                 must have completed already
+  write(res, v) / read(res, v)
+                 a plain shared-memory buffer handed from one role to another:
+                 version v may only be written once version v - 1 was read
 
 Two properties are asserted:
   - every role finishes (no deadlock);
@@ -36,8 +42,9 @@ class Barrier:
 
 
 class Sim:
-    def __init__(self, seed):
+    def __init__(self, seed, preempt=0.25):
         self.rng = random.Random(seed)
+        self.preempt = preempt
         self.bars = {}
         self.pending = []  # (ready_time, seq, barrier) asynchronous arrivals
         self.seq = 0
@@ -48,6 +55,8 @@ class Sim:
         if name not in self.bars:
             self.bars[name] = Barrier(name, count)
         return self.bars[name]
+
+    versions = None  # res -> (last version written, read yet)
 
     def run(self, roles):
         state = {name: None for name in roles}  # pending wait per role
@@ -66,7 +75,12 @@ class Sim:
             name = self.rng.choice(choices)
             gen = live[name]
             state[name] = None
+            first = True
             while True:
+                # a role may be descheduled between any two of its operations
+                if not first and self.rng.random() < self.preempt:
+                    break
+                first = False
                 try:
                     op = next(gen)
                 except StopIteration:
@@ -84,6 +98,25 @@ class Sim:
                         break
                 elif kind == "arrive":
                     self.bars[op[1]].arrive()
+                elif kind == "check":
+                    b, k = op[1], op[2]
+                    assert self.bars[b].completed > k, (
+                        f"{name}: uses data of phase {k} of {b}, which has completed "
+                        f"{self.bars[b].completed}")
+                elif kind in ("write", "read"):
+                    if self.versions is None:
+                        self.versions = {}
+                    res, v = op[1], op[2]
+                    last, seen = self.versions.get(res, (-1, True))
+                    if kind == "write":
+                        assert v == last + 1 and seen, (
+                            f"{name}: writes version {v} of {res} while version {last} "
+                            f"{'was' if seen else 'was not yet'} read")
+                        self.versions[res] = (v, False)
+                    else:
+                        assert v == last and not seen, (
+                            f"{name}: reads version {v} of {res}, which holds {last}")
+                        self.versions[res] = (v, True)
                 elif kind == "commit":
                     issuer = op[2] if len(op) > 2 else name
                     t = max(self.now + self.rng.randint(1, 40), self.last_ready.get(issuer, 0))
@@ -338,6 +371,247 @@ def gemm_pair_roles(sim, tiles, k_blocks, S=6):
             "epi1": epilogue(1), "rel0": release(0), "rel1": release(1)}
 
 
+def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
+    """tk_attn_fwd_kernel (one CTA).  units = list of (n0, n1): the K/V steps
+    of Q tile 0 and Q tile 1 of each unit (n1 = n0 + 1 for a causal diagonal
+    block, n0 = n1 otherwise).  split_p: head dim 64 (P in its own tensor
+    memory columns, one MMA issuer per tile, exponential turns); otherwise
+    head dim 128 (P over S, one issuer for both tiles).  single_fin replays
+    the earlier one-buffer fin_full, and `drop` leaves out one of the
+    softmax's waits ("v_ready", "k_next"), for the negative tests.
+
+    The four softmax warps of a tile, and the four converter warps, act as one
+    role each: their 4-arrival barriers are modelled with one arrival."""
+    S = S or (8 if split_p else 4)
+    QB = QB or (2 if split_p else 1)
+    nissue = 2 if split_p else 1
+    for t in range(2):
+        for b in range(QB):
+            sim.bar(f"q_full{b}_{t}")
+        for name in ("s_full", "p_full", "o_full", "o_free", "s_free", "pv_done", "exp_turn"):
+            sim.bar(f"{name}{t}")
+        for par in range(2):
+            sim.bar(f"fin_full{par}_{t}")
+        sim.bar(f"mma_done{t}")
+    for b in range(QB):
+        sim.bar(f"q_empty{b}", nissue)
+    for s_ in range(S):
+        sim.bar(f"kv_full{s_}"), sim.bar(f"kv_empty{s_}", nissue), sim.bar(f"v_ready{s_}")
+    sim.bar("conv_bar")
+    sim.bars["exp_turn0"].completed = 1  # tile 0 takes the first turn (set at start-up)
+
+    def fin(uc, t):
+        # double-buffered by unit parity; the earlier version had one buffer
+        return (f"fin_full0_{t}", uc) if single_fin else (f"fin_full{uc & 1}_{t}", uc >> 1)
+
+    def producer():
+        kv_idx = 0
+        for uc, (n0, n1) in enumerate(units):
+            qb = uc % QB
+            if uc >= QB:
+                yield ("wait", f"q_empty{qb}", uc // QB - 1)
+            yield ("commit", f"q_full{qb}_0", f"tma_q{qb}")
+            yield ("commit", f"q_full{qb}_1", f"tma_q{qb}")
+            for _ in range(n1):
+                for _kv in range(2):
+                    s_, fill = kv_idx % S, kv_idx // S
+                    if fill > 0:
+                        yield ("wait", f"kv_empty{s_}", fill - 1)
+                    yield ("commit", f"kv_full{s_}", f"tma{s_}")  # loads land in any order
+                    kv_idx += 1
+        # load_exit: the last fill of every stage and the last load of each Q buffer
+        for s_ in range(min(S, kv_idx)):
+            last = kv_idx - 1 - ((kv_idx - 1 - s_) % S)
+            yield ("wait", f"kv_full{s_}", last // S)
+        nq = len(units)
+        for b in range(min(QB, nq)):
+            last = nq - 1 - ((nq - 1 - b) % QB)
+            yield ("wait", f"q_full{b}_0", last // QB)
+            yield ("wait", f"q_full{b}_1", last // QB)
+
+    def softmax(t):
+        steps = turns = kvb = 0
+        s_waits = 0
+        for uc, (n0, n1) in enumerate(units):
+            n_t = n1 if t else n0
+            for j in range(n_t):
+                yield ("wait", f"s_full{t}", s_waits)
+                s_waits += 1
+                if split_p:
+                    yield ("arrive", f"s_free{t}")
+                take_turn = split_p and (t == 0 or j < n0)
+                if take_turn:
+                    yield ("wait", f"exp_turn{t}", turns)
+                    turns += 1
+                    yield ("arrive", f"exp_turn{t ^ 1}")
+                if split_p:
+                    if steps > 0:
+                        yield ("wait", f"pv_done{t}", steps - 1)
+                    steps += 1
+                vidx = kvb + 2 * j + 1
+                if "v_ready" not in drop:
+                    yield ("wait", f"v_ready{vidx % S}", vidx // S)
+                if j == n_t - 1:
+                    yield ("write", f"fin{uc & 1 if not single_fin else 0}_{t}",
+                           uc >> 1 if not single_fin else uc)
+                if not split_p and j + 1 < n_t and "k_next" not in drop:
+                    kidx = kvb + 2 * (j + 1)
+                    yield ("wait", f"kv_full{kidx % S}", kidx // S)
+                yield ("arrive", f"p_full{t}")
+                if j == n_t - 1:
+                    yield ("arrive", fin(uc, t)[0])
+            kvb += 2 * n1
+
+    def converter():
+        kvb = conv = 0
+        pend = None
+        for uc in range(len(units) + 1):
+            have = uc < len(units)
+            n1 = units[uc][1] if have else 0
+            for j in range(n1 + 1):
+                if pend is not None and (j == 1 or not have):
+                    for t in range(2):
+                        bar, k = fin(pend, t)
+                        yield ("wait", bar, k)
+                        yield ("wait", f"o_full{t}", pend)
+                        yield ("read", f"fin{pend & 1 if not single_fin else 0}_{t}",
+                               pend >> 1 if not single_fin else pend)
+                        yield ("arrive", f"o_free{t}")
+                    pend = None
+                if j == n1:
+                    break
+                vidx = kvb + 2 * j + 1
+                st = vidx % S
+                yield ("wait", f"kv_full{st}", vidx // S)
+                yield ("arrive", "conv_bar")  # the four warps agree on the tile's range
+                yield ("wait", "conv_bar", conv)
+                conv += 1
+                yield ("arrive", f"v_ready{st}")
+            if not have:
+                break
+            pend = uc
+            kvb += 2 * n1
+
+    def mma_split(t):
+        p_cnt = s_cnt = kvb = 0
+        for uc, (n0, n1) in enumerate(units):
+            n_t = n1 if t else n0
+            qb = uc % QB
+            for j in range(n1 + 1):
+                kidx = kvb + 2 * j
+                vidx = kidx - 1
+                ks, vs = kidx % S, vidx % S
+                do_s, do_pv = j < n_t, 1 <= j <= n_t
+                if do_s:
+                    yield ("wait", f"kv_full{ks}", kidx // S)
+                    if j == 0:
+                        yield ("wait", f"q_full{qb}_{t}", uc // QB)
+                    if s_cnt > 0:
+                        yield ("wait", f"s_free{t}", s_cnt - 1)
+                    s_cnt += 1
+                    yield ("commit", f"s_full{t}")
+                if do_pv:
+                    if j == 1 and uc > 0:
+                        yield ("wait", f"o_free{t}", uc - 1)
+                    yield ("wait", f"p_full{t}", p_cnt)
+                    p_cnt += 1
+                    yield ("check", f"v_ready{vs}", vidx // S)  # V_{j-1} converted
+                    yield ("commit", f"pv_done{t}")
+                    if j == n_t:
+                        yield ("commit", f"o_full{t}")
+                if j < n1:
+                    yield ("commit", f"kv_empty{ks}")
+                if j >= 1:
+                    yield ("commit", f"kv_empty{vs}")
+                if j == n1 - 1:
+                    yield ("commit", f"q_empty{qb}")
+            kvb += 2 * n1
+        yield ("commit", f"mma_done{t}")
+        yield ("wait", f"mma_done{t}", 0)
+
+    def mma_shared():
+        p_cnt = [0, 0]
+        kvb = 0
+        for uc, (n0, n1) in enumerate(units):
+            for j in range(n1 + 1):
+                kidx = kvb + 2 * j
+                vidx = kidx - 1
+                ks, vs = kidx % S, vidx % S
+                k_ready = False
+                for t in range(2):
+                    n_t = n1 if t else n0
+                    do_pv, do_s = 1 <= j <= n_t, j < n_t
+                    if do_pv:
+                        if j == 1 and uc > 0:
+                            yield ("wait", f"o_free{t}", uc - 1)
+                        yield ("wait", f"p_full{t}", p_cnt[t])
+                        p_cnt[t] += 1
+                    if do_s and (j == 0 or not do_pv):
+                        if j == 0:
+                            yield ("wait", f"q_full0_{t}", uc)
+                        if not k_ready:
+                            yield ("wait", f"kv_full{ks}", kidx // S)
+                        k_ready = True
+                    if do_pv:
+                        yield ("check", f"v_ready{vs}", vidx // S)  # V_{j-1} converted
+                    if do_s:
+                        yield ("check", f"kv_full{ks}", kidx // S)  # K_j landed
+                        yield ("commit", f"s_full{t}")
+                    if do_pv and j == n_t:
+                        yield ("commit", f"o_full{t}")
+                if j < n1:
+                    yield ("commit", f"kv_empty{ks}")
+                if j >= 1:
+                    yield ("commit", f"kv_empty{vs}")
+                if j == n1 - 1:
+                    yield ("commit", "q_empty0")
+            kvb += 2 * n1
+        yield ("commit", "mma_done0")
+        yield ("wait", "mma_done0", 0)
+
+    roles = {"producer": producer(), "softmax0": softmax(0), "softmax1": softmax(1),
+             "converter": converter()}
+    if split_p:
+        roles["mma0"], roles["mma1"] = mma_split(0), mma_split(1)
+    else:
+        roles["mma"] = mma_shared()
+    return roles
+
+
+FWD_UNITS = [
+    [(1, 1)], [(1, 2)], [(2, 2)], [(4, 4)],
+    [(1, 2), (1, 2), (1, 2)],              # single-step causal units, back to back
+    [(1, 1), (1, 1), (1, 1), (1, 1)],
+    [(3, 4), (1, 2), (5, 6), (2, 3)],       # causal, mixed lengths
+    [(6, 6), (2, 2), (9, 9)],
+    [(1, 2), (7, 8), (1, 2), (1, 2), (3, 4)],
+]
+
+
+@pytest.mark.parametrize("units", FWD_UNITS,
+                         ids=lambda u: "-".join(f"{a}.{b}" for a, b in u))
+@pytest.mark.parametrize("split_p", [True, False], ids=["d64_split_p", "d128_shared_sp"])
+def test_forward_protocol(split_p, units):
+    for seed in range(80):
+        sim = Sim(seed)
+        sim.run(fwd_roles(sim, units, split_p))
+
+
+@pytest.mark.parametrize("split_p", [True, False], ids=["d64_split_p", "d128_shared_sp"])
+def test_forward_single_fin_buffer_runs_ahead(split_p):
+    """The race the double-buffered fin_full fixed: with one buffer per tile,
+    a unit whose tile 0 takes a single step can publish its final row max and
+    sum before the epilogue of the previous unit has read them."""
+    failures = 0
+    for seed in range(300):
+        sim = Sim(seed)
+        try:
+            sim.run(fwd_roles(sim, [(1, 2)] * 5, split_p, single_fin=True))
+        except AssertionError:
+            failures += 1
+    assert failures > 0
+
+
 @pytest.mark.parametrize("tiles,k_blocks", [(1, 1), (1, 7), (2, 3), (3, 1), (5, 4), (4, 13)])
 def test_gemm_pair_protocol(tiles, k_blocks):
     for seed in range(60):
@@ -388,5 +662,22 @@ def test_single_s_barrier_for_two_buffers_runs_ahead():
         try:
             sim.run(roles(sim))
         except AssertionError:
+            failures += 1
+    assert failures > 0
+
+
+@pytest.mark.parametrize("split_p,drop", [(True, "v_ready"), (False, "v_ready"),
+                                          (False, "k_next")])
+def test_forward_model_sees_a_missing_wait(split_p, drop):
+    """The data checks are live: without the softmax's wait for the converted
+    V tile (or, with P over S, for the next K tile), the MMA thread issues a
+    product whose operand has not landed in some interleavings."""
+    failures = 0
+    for seed in range(300):
+        sim = Sim(seed)
+        try:
+            sim.run(fwd_roles(sim, [(3, 4), (2, 3), (4, 4)], split_p, drop=(drop,)))
+        except AssertionError as e:
+            assert "uses data" in str(e) or "completed" in str(e), str(e)
             failures += 1
     assert failures > 0
