@@ -420,6 +420,16 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// x rounded to the nearest fp16 value (ties to even), as fp32: the value the
+// tensor core sees for an element packed by pack_f16x2.
+__device__ __forceinline__ float round_to_f16(float x) {
+  unsigned short h;
+  float r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(x));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(h));
+  return r;
+}
+
 // Per-16-bit-lane unsigned max.
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   uint32_t r;

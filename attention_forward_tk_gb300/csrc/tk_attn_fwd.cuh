@@ -34,13 +34,17 @@
 //   by the same thread, and one thread's MMAs run in issue order.
 //
 // Precision: S = Q K^T in bf16 x bf16 -> fp32.  P is rounded to fp16
-// (2^-12 relative, eight times finer than bf16) and multiplied with V in
-// fp16 x fp16 -> fp32; each V tile is converted exactly to fp16 in shared
-// memory, scaled by a power of two 2^E when its magnitudes would overflow
-// fp16 (E is non-increasing along a unit and O is rescaled to match, so the
-// scaling is exact).  The running max is lazy: a row's reference max moves
-// only when the tile max exceeds it by more than 2^8 (log2 units), so P <=
-// 256 and O needs rescaling rarely; the row sum l is accumulated in fp32.
+// (at most 2^-11 relative, eight times finer than bf16) and multiplied with
+// V in fp16 x fp16 -> fp32; each V tile is converted exactly to fp16 in
+// shared memory, scaled by a power of two 2^E when its magnitudes would
+// overflow fp16 (E is non-increasing along a unit and O is rescaled to
+// match, so the scaling is exact).  The running max is lazy: a row's
+// reference max moves only when the tile max exceeds it by more than 2^8
+// (log2 units), so P <= 256 and O needs rescaling rarely.  The row sum l is
+// accumulated in fp32 from the unrounded P, and gives the LSE.  O is divided
+// by l plus the fp16 rounding error of each tile's largest P: in a row that
+// one key dominates, numerator and denominator then carry the same rounded
+// weight, and the dominant value passes through without the 2^-11 error.
 //
 // Every wait on an mbarrier is bounded; a wait that runs out raises a shared
 // abort flag (all roles then leave their loops), records an error code in a
@@ -151,6 +155,7 @@ struct FwdShared {
   uint32_t conv_max[2][4];
   float m_fin[2][2][128];  // [unit parity][tile][row] final reference max (scaled log2)
   float l_fin[2][2][128];  // [unit parity][tile][row] final row sum
+  float lc_fin[2][2][128]; // [unit parity][tile][row] fp16 rounding of the tile maxima's P
   uint64_t s_free[2];     // softmax has read S_t (split P only) (4 softmax warps)
   uint64_t pv_done[2];    // P_t V MMA complete (split P only)  (commit)
   uint64_t exp_turn[2];   // split P: tile t may run its exponentials (4 warps of the other tile)
@@ -325,6 +330,7 @@ __global__ void __launch_bounds__(512, 1)
       const int n_t = t ? n1 : n0;
       const int qrow = mb * 256 + t * 128 + row;  // global query index
       float m_run = -INFINITY, l_run = 0.f;
+      float lc_run = 0.f;  // sum of (fp16(P) - P) over each tile's largest P
       int e_cur = 0;  // V exponent O is accumulated at
       for (int j = 0; j < n_t; ++j) {
         if (!mbar_wait(&sb.s_full[t], s_phase, abort_flag)) {
@@ -367,14 +373,19 @@ __global__ void __launch_bounds__(512, 1)
           for (int q = 0; q < 8; ++q)
             mx[q] = max3(mx[q], __uint_as_float(s[i + 2 * q]), __uint_as_float(s[i + 2 * q + 1]));
         }
-        const float m_cand =
-            fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], max3(mx[5], mx[6], mx[7]))) * c;
+        const float s_max =
+            fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], max3(mx[5], mx[6], mx[7])));
+        const float m_cand = s_max * c;
         // Lazy max: move the reference only when the tile max exceeds it by
         // more than kTau (always on the first tile, where m_run = -inf).
         const bool grow = m_cand > m_run + kTau;
         const float m_new = grow ? m_cand : m_run;
         const float fac = grow ? ex2_approx(m_run - m_new) : 1.0f;  // 0 on the first tile
         m_run = m_new;
+        // The tile's largest P exactly as the loop below computes it, and the
+        // error its fp16 rounding puts into the P V product.
+        const float p_max = ex2_approx(fmaf(s_max, c, -m_run));
+        const float p_max_err = round_to_f16(p_max) - p_max;
         // P = 2^(s*c - m_run) <= 2^kTau, rounded to fp16 for the P V MMA;
         // the row sum is taken over the fp32 P.
         const uint64_t c2 = f2_pack(c, c);
@@ -467,20 +478,12 @@ __global__ void __launch_bounds__(512, 1)
           float a0, a1;
           f2_unpack(f2_add(la, lb), a0, a1);
           l_run = l_run * fac + (a0 + a1);
+          lc_run = lc_run * fac + p_max_err;
         }
         if (j == n_t - 1) {
           sb.m_fin[uc & 1][t][row] = m_run;
           sb.l_fin[uc & 1][t][row] = l_run;
-        }
-        // Shared S/P: the MMA thread's next group for this tile is
-        // [P_t V_j, S_t = Q_t K_{j+1}^T] and it waits only for this signal:
-        // make sure K_{j+1} has landed (V_j is converted: waited above).
-        if (!C::kSplitP && j + 1 < n_t) {
-          const uint32_t kidx = kvb + 2 * (j + 1);
-          if (!mbar_wait(&sb.kv_full[kidx % C::kStages], (kidx / C::kStages) & 1, abort_flag)) {
-            raise_abort(sb, p.err, kDevErrTimeout);
-            goto done;
-          }
+          sb.lc_fin[uc & 1][t][row] = lc_run;
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after_sync();
             const float m = sb.m_fin[pend_uc & 1][t][row];
             const float l = sb.l_fin[pend_uc & 1][t][row];
-            const float oscale = exp2i(-pend_e[t]) / l;
+            const float oscale = exp2i(-pend_e[t]) / (l + sb.lc_fin[pend_uc & 1][t][row]);
             const int qrow = pend_mb * 256 + t * 128 + row;
             const bool valid = qrow < p.N;
             const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
@@ -765,9 +768,11 @@ __global__ void __launch_bounds__(512, 1)
       // S0 = Q0 K_j^T, then P1 V_{j-1}, S1 = Q1 K_j^T, so each softmax
       // warpgroup works while the other tile's two MMAs run, and a tile's
       // scores complete as one group (two independent issuers would
-      // interleave the tiles' MMAs and delay both).  One wait per tile and
-      // step: the softmax signals P_t only once V_{j-1} is converted and K_j
-      // has landed.
+      // interleave the tiles' MMAs and delay both).  The softmax signals P_t
+      // only once V_{j-1} is converted; this thread checks that K_j has
+      // landed (one probe per step, usually already complete).  Keeping that
+      // check here rather than in the softmax shortens the softmax's step by
+      // a barrier probe: +4% on the causal workloads.
       constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);  // bf16 Q, K
       constexpr uint32_t idO = idesc_f32acc(false, 128, D, false, true);    // fp16 P, V
       // Descriptor words: the low word carries the address / 16, stepped by
@@ -797,9 +802,8 @@ __global__ void __launch_bounds__(512, 1)
             const bool do_s = j < n_t;
             const uint32_t tS = tmem + (t ? C::kColS1 : C::kColS0);
             const uint32_t tO = tmem + (t ? C::kColO1 : C::kColO0);
-            // One wait per group on the steady path: the softmax signals P_t
-            // only after V_{j-1} is converted and K_j has landed (see there).
-            // The first S of a unit waits for its Q tile and K_0 here.
+            // The softmax signals P_t only after V_{j-1} is converted; K_j and
+            // (for a unit's first S) the Q tile are waited for here.
             if (do_pv) {
               if ((j == 1 && uc > 0 && !mbar_wait(&sb.o_free[t], (uc - 1) & 1, abort_flag)) ||
                   !mbar_wait(&sb.p_full[t], p_phase[t], abort_flag)) {
@@ -808,7 +812,7 @@ __global__ void __launch_bounds__(512, 1)
               }
               p_phase[t] ^= 1;
             }
-            if (do_s && (j == 0 || !do_pv)) {
+            if (do_s) {
               if ((j == 0 && !mbar_wait(&sb.q_full[0][t], uc & 1, abort_flag)) ||
                   (!k_ready && !mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag))) {
                 raise_abort(sb, p.err, kDevErrTimeout);

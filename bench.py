@@ -14,9 +14,13 @@ beside it.
 
 One step = one tk_attn_fwd call (the whole hot path: TMA loads, QK^T,
 online softmax, PV, epilogue) over one batch of synthetic inputs resident in
-HBM.  The default workload is B16 H16 N1024 D64 non-causal; the metric is
-TFLOP/s with F = 4*B*H*N^2*D (halved under the causal mask) and its fraction
-of the measured dense bf16 tensor peak.  L2 (126 MB) is flushed by writing a
+HBM.  The default workload is the largest one, B4 H32 N16384 D128 causal
+(peaky scores, Student-t values); the metric is TFLOP/s with
+F = 4*B*H*N^2*D (halved under the causal mask) and its fraction of the
+measured dense bf16 tensor peak.  The same run also times the other
+D = 128 workloads (B16 H16 N4096 non-causal, B8 H16 N8192 causal) and the
+short-sequence one (B16 H16 N1024 D64, with its HBM GB/s), each with its own
+clock record, under the key "other_configs".  L2 (126 MB) is flushed by writing a
 256 MB buffer before every timed step; each step is timed with CUDA events on
 the launching stream.  Rank 0 prints one JSON line.
 
@@ -43,7 +47,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "n1024_d64"
+DEFAULT_WORKLOAD = "n16384_d128_c"
+# timed beside the default workload in every run, each with its own clock record
+COMPANION_WORKLOADS = ("n4096_d128", "n8192_d128_c", "n1024_d64")
 L2_FLUSH_BYTES = 256 << 20
 # Device code of the forward kernel: recorded DRAM traffic is valid while
 # these files are unchanged.
@@ -165,6 +171,36 @@ def reduce_max(values, world: int, device=None):
 def job_throughput(world: int, flops_per_step: float, steps: int, seconds: float) -> float:
     """TFLOP/s of the whole job: the work of all ranks over the slowest rank's time."""
     return world * flops_per_step * steps / seconds / 1e12
+
+
+def config_of(w, world: int) -> dict:
+    """The `config` object of a JSON line; both arms print the same one."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.keys, "D": w.D,
+            "causal": w.causal, "values": w.dist, "flops_per_step": w.flops,
+            "l2": "flushed (256 MB write) before every timed step",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            key, _, val = line.partition(":")
+            if key.strip() == "Model name" and val.strip() and val.strip() != "-":
+                return val.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip() in ("model name", "Model", "Hardware") and val.strip():
+                    return val.strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -461,6 +497,8 @@ def main():
                     help="GEMM workload: skip the cuBLAS comparison (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--no-companions", action="store_true",
+                    help="skip the other workloads timed beside the main one (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -523,6 +561,31 @@ def main():
         (e2e_ms,) = reduce_max([e2e_ms], world, device)
     e2e_value = job_throughput(world, w.flops, 1, e2e_ms / 1e3)
 
+    peak_tf, peak_hbm, peak_kind = measured_peaks()
+    companions = {}
+    if not args.all_workloads and not args.no_companions:
+        for name in COMPANION_WORKLOADS:
+            if name == w.name:
+                continue
+            cw = BY_NAME[name]
+            # enough launches for about half a second, so the clock sampler
+            # sees the workload run
+            probe, _, _ = time_gpu(cw, 3, 3, device)
+            n = int(min(400, max(20, 500.0 / max(statistics.median(probe), 1e-3))))
+            with ClockSampler(device.index if world == 1 else local) as cclk:
+                cms, _, _ = time_gpu(cw, n, 3, device)
+            (cmean,) = reduce_max([statistics.mean(cms)], world, device)
+            c = cclk.summary()
+            tf = world * cw.flops / cmean / 1e9
+            companions[name] = {
+                "ms_mean": round(cmean, 5), "ms_median": round(statistics.median(cms), 5),
+                "value": round(tf, 2), "unit": "TFLOP/s",
+                "frac_of_bf16_peak": round(tf / world / peak_tf, 4),
+                "hbm_gbs": round(cw.io_bytes / cmean / 1e6, 1),
+                "frac_of_hbm_peak": round(cw.io_bytes / cmean / 1e6 / peak_hbm, 4),
+                "launches": n, "config": config_of(cw, world),
+                "clocks": c}
+
     extra = {}
     if args.all_workloads:
         for ow in WORKLOADS + EXTRA_WORKLOADS:
@@ -568,7 +631,6 @@ def main():
             dist.destroy_process_group()
         return
 
-    peak_tf, peak_hbm, peak_kind = measured_peaks()
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
     hbm_gbs = w.io_bytes / (kernel_ms / 1e3) / 1e9
     # the binding roofline: the tensor cores, unless moving the algorithmic
@@ -588,10 +650,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.keys, "D": w.D,
-                   "causal": w.causal, "values": w.dist, "flops_per_step": w.flops,
-                   "l2": "flushed (256 MB write) before every timed step",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": config_of(w, world),
         "roofline": ({"bound": "hbm", "achieved": round(hbm_gbs, 1),
                       "peak": peak_hbm, "unit": "GB/s",
                       "frac": round(hbm_gbs / peak_hbm, 4),
@@ -615,12 +674,14 @@ def main():
     }
     line["roofline"]["traffic"] = traffic
     line["roofline"]["algorithmic_bytes"] = w.io_bytes
+    if companions:
+        line["other_configs"] = companions
     if extra:
         line["all_workloads"] = extra
     if not args.no_cpu_baseline and world >= 1:
         tf, threads, n, dt = cpu_oracle_sample(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads,
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu_model": cpu_model(),
                                 "sample": f"{n} random rows of {w.name}, fp64, {dt:.1f} s"}
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -755,9 +816,9 @@ def main_reference(args, w, world, rank):
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.keys, "D": w.D,
-                   "causal": w.causal, "values": w.dist, "flops_per_step": w.flops},
+        "config": config_of(w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"{samples[0][1]} random rows of {w.name} per step "
                                    f"(~{per_step:.0f} s of fp64 work)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

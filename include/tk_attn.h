@@ -34,6 +34,11 @@
  *     never synchronises the stream (except tk_attn_last_device_error).  Work
  *     is enqueued on `stream` (0 = the legacy default stream) and runs
  *     asynchronously; results are valid once the stream reaches that point.
+ *   - One exception, once per device: the first call of any entry point on a
+ *     device sets that device up (kernel attributes, the address of the
+ *     device error word, which it clears with cudaMemset) and ends with
+ *     cudaDeviceSynchronize.  Make that first call before any stream
+ *     capture; later calls never synchronise.
  *   - Return value: TK_ATTN_OK (0) or a negative TK_ATTN_ERR_* code.  On any
  *     error no work is enqueued and the outputs are left untouched.
  *   - Thread safety: calls may come from several host threads; cached host
@@ -82,8 +87,9 @@ typedef struct CUstream_st *tk_attn_stream_t;
  *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i
  *   stream   CUDA stream to enqueue on
  *
- * Limits: B*H*N*D must stay below 2^31 elements per tensor map dimension
- * product (checked), N < 2^31.
+ * Limits (checked before any CUDA call, else TK_ATTN_ERR_UNSUPPORTED):
+ * B*H < 2^31 and B*H*ceil(N/256) < 2^31 (work units); each of q, k, v and o
+ * below 2^40 bytes (the tensor map's stride range).
  * Errors: TK_ATTN_ERR_INVALID_ARG, _UNSUPPORTED, _ARCH, _LAUNCH (see above).
  */
 int tk_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,

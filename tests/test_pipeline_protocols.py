@@ -377,8 +377,9 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
     block, n0 = n1 otherwise).  split_p: head dim 64 (P in its own tensor
     memory columns, one MMA issuer per tile, exponential turns); otherwise
     head dim 128 (P over S, one issuer for both tiles).  single_fin replays
-    the earlier one-buffer fin_full, and `drop` leaves out one of the
-    softmax's waits ("v_ready", "k_next"), for the negative tests.
+    the earlier one-buffer fin_full, and `drop` leaves out the softmax's
+    wait for the converted V tile ("v_ready") or, with P over S, the MMA
+    thread's wait for the K tile ("k_wait"), for the negative tests.
 
     The four softmax warps of a tile, and the four converter warps, act as one
     role each: their 4-arrival barriers are modelled with one arrival."""
@@ -454,9 +455,6 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
                 if j == n_t - 1:
                     yield ("write", f"fin{uc & 1 if not single_fin else 0}_{t}",
                            uc >> 1 if not single_fin else uc)
-                if not split_p and j + 1 < n_t and "k_next" not in drop:
-                    kidx = kvb + 2 * (j + 1)
-                    yield ("wait", f"kv_full{kidx % S}", kidx // S)
                 yield ("arrive", f"p_full{t}")
                 if j == n_t - 1:
                     yield ("arrive", fin(uc, t)[0])
@@ -546,10 +544,10 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
                             yield ("wait", f"o_free{t}", uc - 1)
                         yield ("wait", f"p_full{t}", p_cnt[t])
                         p_cnt[t] += 1
-                    if do_s and (j == 0 or not do_pv):
+                    if do_s:
                         if j == 0:
                             yield ("wait", f"q_full0_{t}", uc)
-                        if not k_ready:
+                        if not k_ready and "k_wait" not in drop:
                             yield ("wait", f"kv_full{ks}", kidx // S)
                         k_ready = True
                     if do_pv:
@@ -667,11 +665,12 @@ def test_single_s_barrier_for_two_buffers_runs_ahead():
 
 
 @pytest.mark.parametrize("split_p,drop", [(True, "v_ready"), (False, "v_ready"),
-                                          (False, "k_next")])
+                                          (False, "k_wait")])
 def test_forward_model_sees_a_missing_wait(split_p, drop):
     """The data checks are live: without the softmax's wait for the converted
-    V tile (or, with P over S, for the next K tile), the MMA thread issues a
-    product whose operand has not landed in some interleavings."""
+    V tile (or, with P over S, the MMA thread's wait for the K tile), the MMA
+    thread issues a product whose operand has not landed in some
+    interleavings."""
     failures = 0
     for seed in range(300):
         sim = Sim(seed)

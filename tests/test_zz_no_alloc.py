@@ -1,9 +1,12 @@
 """The no-allocation entry point, tk_attn_fwd_splitkv_static, through the C
 ABI: the split over keys with its partial results in the library's static
-scratch instead of a caller workspace.  Checked against tk_attn_fwd_splitkv
-(the same computation with a torch-allocated workspace) on two calls in a
-row, within the parity tolerances (max |dO| <= 2e-2, max |dLSE| <= 1e-3),
-and its rejection of a split whose partial results exceed the scratch.
+scratch instead of a caller workspace.  Checked on two calls in a row
+against tk_attn_fwd_splitkv (the same computation with a torch-allocated
+workspace: the outputs must be bit-identical) and against the fp64 oracle
+within the parity tolerances (max |dO| <= 2e-2, mean |dO| <= 2e-3,
+max |dLSE| <= 1e-3).  Warmed-up calls must leave the device's free memory
+and torch's allocator statistics unchanged.  Also checked: its rejection of
+a split whose partial results exceed the scratch.
 
 This file is collected last, so a run that stops at the first failure has
 already run every other test; it passes alone in a fresh process as well.
@@ -12,7 +15,7 @@ import numpy as np
 import pytest
 import torch
 
-from conftest import TOL_LSE_MAX, TOL_O_MAX
+from conftest import TOL_LSE_MAX, TOL_O_MAX, TOL_O_MEAN
 
 pytestmark = pytest.mark.gpu
 
@@ -20,12 +23,13 @@ SCRATCH_BYTES = 64 << 20
 
 
 def inputs(B, H, Nq, Nk, D, seed):
+    """Host (CPU) and device copies of q, k, v ~ N(0, 1), bf16."""
     g = torch.Generator().manual_seed(seed)
     dev = torch.device("cuda", 0)
-    q = torch.randn((B, H, Nq, D), generator=g).to(torch.bfloat16).to(dev)
-    k = torch.randn((B, H, Nk, D), generator=g).to(torch.bfloat16).to(dev)
-    v = torch.randn((B, H, Nk, D), generator=g).to(torch.bfloat16).to(dev)
-    return q, k, v
+    host = (torch.randn((B, H, Nq, D), generator=g).to(torch.bfloat16),
+            torch.randn((B, H, Nk, D), generator=g).to(torch.bfloat16),
+            torch.randn((B, H, Nk, D), generator=g).to(torch.bfloat16))
+    return host, tuple(t.to(dev) for t in host)
 
 
 def outputs(q):
@@ -37,31 +41,44 @@ def outputs(q):
 
 @pytest.mark.parametrize("shape", [(1, 8, 256, 8192, 128, 0), (2, 3, 100, 3000, 64, 5)],
                          ids=["B1H8q256k8192d128", "B2H3q100k3000d64s5"])
-def test_static_scratch_matches_workspace_call_twice(tk_lib, shape):
+def test_static_scratch_matches_workspace_call_twice(tk_lib, oracle_lib, shape):
     B, H, Nq, Nk, D, splits = shape
-    q, k, v = inputs(B, H, Nq, Nk, D, seed=700 + Nq)
+    scale = 0.1
+    (qh, kh, vh), (q, k, v) = inputs(B, H, Nq, Nk, D, seed=700 + Nq)
     stream = torch.cuda.current_stream().cuda_stream
     need = tk_lib.tk_attn_splitkv_workspace_bytes(B, H, Nq, Nk, D, splits)
     assert 0 < need <= SCRATCH_BYTES
     ws = torch.empty(need, dtype=torch.uint8, device=q.device)
     o_ref, l_ref = outputs(q)
     st = tk_lib.tk_attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_ref.data_ptr(),
-                                    l_ref.data_ptr(), B, H, Nq, Nk, D, 0.1, splits,
+                                    l_ref.data_ptr(), B, H, Nq, Nk, D, scale, splits,
                                     ws.data_ptr(), need, stream)
     assert st == 0, tk_lib.tk_attn_status_string(st)
-    for call in range(2):  # two calls in a row share (and reuse) the scratch
-        o, lse = outputs(q)
+    o_ora, l_ora = oracle_lib.attention_qk(qh, kh, vh, scale, False)
+    results = [outputs(q) for _ in range(2)]
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved())
+    for o, lse in results:  # two calls in a row share (and reuse) the scratch
         st = tk_lib.tk_attn_fwd_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                                o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, D,
-                                               0.1, splits, stream)
+                                               scale, splits, stream)
         assert st == 0, tk_lib.tk_attn_status_string(st)
-        assert tk_lib.tk_attn_last_device_error(stream) == 0
         torch.cuda.synchronize()
-        do = (o.float() - o_ref.float()).abs()
-        dl = (lse - l_ref).abs()
+    # the calls allocated nothing on the device, through torch or around it
+    free1, _ = torch.cuda.mem_get_info()
+    assert (torch.cuda.memory_allocated(), torch.cuda.memory_reserved()) == stats0
+    assert free1 == free0
+    assert tk_lib.tk_attn_last_device_error(stream) == 0
+    for call, (o, lse) in enumerate(results):
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-        assert do.max().item() <= TOL_O_MAX, (call, do.max().item())
-        assert dl.max().item() <= TOL_LSE_MAX, (call, dl.max().item())
+        # the same kernels and the same split as the workspace call: identical bits
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref), call
+        do = np.abs(o.float().cpu().double().numpy() - o_ora)
+        dl = np.abs(lse.cpu().double().numpy() - l_ora)
+        assert do.max() <= TOL_O_MAX, (call, do.max())
+        assert do.mean() <= TOL_O_MEAN, (call, do.mean())
+        assert dl.max() <= TOL_LSE_MAX, (call, dl.max())
 
 
 def test_static_scratch_rejects_a_split_beyond_it(tk_lib):
