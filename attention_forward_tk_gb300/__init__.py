@@ -24,6 +24,7 @@ from .api import (  # noqa: F401
     tk_attn_bwd_workspace_bytes,
     tk_attn_check_args,
     tk_attn_fwd,
+    tk_attn_fwd_qk,
     tk_attn_fwd_splitkv,
     tk_attn_last_device_error,
     tk_attn_splitkv_workspace_bytes,

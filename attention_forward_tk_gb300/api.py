@@ -32,6 +32,7 @@ TK_ATTN_ERR_TOO_LARGE = -6
 EXPORTED = (
     "tk_attn_fwd",
     "tk_attn_fwd_splitkv",
+    "tk_attn_fwd_qk",
     "tk_attn_fwd_splitkv_static",
     "tk_attn_splitkv_workspace_bytes",
     "tk_attn_check_args",
@@ -81,6 +82,9 @@ def library() -> ctypes.CDLL:
         lib.tk_attn_fwd_splitkv.restype = i
         lib.tk_attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
                                             ctypes.c_size_t, vp]
+        lib.tk_attn_fwd_qk.restype = i
+        lib.tk_attn_fwd_qk.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
+                                       ctypes.c_size_t, vp]
         lib.tk_attn_fwd_splitkv_static.restype = i
         lib.tk_attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.tk_attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
@@ -130,6 +134,14 @@ def tk_attn_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int
     return int(library().tk_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, D,
                                              ctypes.c_float(scale), int(num_splits), workspace,
                                              int(workspace_bytes), stream))
+
+
+def tk_attn_fwd_qk(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Nq: int, Nk: int,
+                   D: int, scale: float, causal: int, num_splits: int, workspace: int,
+                   workspace_bytes: int, stream: int) -> int:
+    return int(library().tk_attn_fwd_qk(q, k, v, o, lse, B, H, Nq, Nk, D, ctypes.c_float(scale),
+                                        int(causal), int(num_splits), workspace,
+                                        int(workspace_bytes), stream))
 
 
 def tk_attn_fwd_splitkv_static(q: int, k: int, v: int, o: int, lse: int, B: int, H: int,
@@ -261,11 +273,14 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
 
 
 def attention_forward_splitkv(q, k, v, scale: float | None = None, num_splits: int = 0,
-                              out=None, lse=None, workspace=None, stream=None):
+                              out=None, lse=None, workspace=None, stream=None,
+                              causal: bool = False):
     """O, LSE for bf16 CUDA tensors q [B, H, Nq, D] against k, v [B, H, Nk, D],
-    unmasked, with the keys split into `num_splits` ranges (0: the library's
-    default).  The workspace is allocated by torch when not given.  Enqueued
-    on `stream`; returns immediately.
+    with the keys split into `num_splits` ranges (0: the library's default).
+    causal: key j visible to query i iff j <= i + Nk - Nq (the queries are
+    the sequence's last Nq positions; tk_attn_fwd_qk).  The workspace is
+    allocated by torch when not given.  Enqueued on `stream`; returns
+    immediately.
     """
     import torch
     if q.dim() != 4 or k.shape != v.shape or k.dim() != 4 or q.shape[:2] != k.shape[:2] or \
@@ -287,9 +302,9 @@ def attention_forward_splitkv(q, k, v, scale: float | None = None, num_splits: i
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else 0
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(tk_attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                               lse.data_ptr(), B, H, Nq, Nk, D, float(scale), int(num_splits),
-                               ws_ptr, ws_bytes, _stream_handle(stream)))
+    _check(tk_attn_fwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, H, Nq, Nk, D, float(scale), int(bool(causal)),
+                          int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream)))
     return out, lse
 
 

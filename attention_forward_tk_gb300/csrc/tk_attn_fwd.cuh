@@ -70,19 +70,25 @@ struct FwdParams {
   int *err;          // device error word
   int BH;            // batch * heads
   int N;             // query rows per slice (Nq)
-  int Nk;            // keys per slice (== N except for the split-key call)
+  int Nk;            // keys per slice (== N except for the queries-vs-keys calls)
+  int q_off;         // causal: absolute position of query row 0 (Nk - Nq; key j is
+                     // visible to query i iff j <= i + q_off)
   int num_mblocks;   // ceil(N / 256)
   int num_units;     // BH * num_mblocks
   float scale_log2;  // scale * log2(e)
   int test_drop_load;  // test hook: CTA 0 skips its first K load (0 = off)
   int head_group;      // causal unit order: heads per section (>= 1)
-  // Split over keys (inference shape, unmasked): every (slice, 256-query
-  // block) is cut into num_splits ranges of split_tiles 128-key tiles; a unit
-  // writes its range's O / l (fp32) and natural-log LSE to o_part
-  // [num_splits, BH, N, D] and lse_part [num_splits, BH, N], which a second
-  // kernel combines.
+  // Split over keys (inference shape): every (slice, 256-query block) is cut
+  // into ranges of split_tiles 128-key tiles; a unit writes its range's O / l
+  // (fp32) and natural-log LSE to o_part [num_splits, BH, N, D] and lse_part
+  // [num_splits, BH, N], which a second kernel combines.  Unmasked: every
+  // block has num_splits ranges.  Causal: block mb has
+  // ceil(kv_tiles(mb, 0) / split_tiles) ranges (at most num_splits), the last
+  // of which also holds the key tiles only the block's second Q tile sees;
+  // units_per_bh counts them over the blocks of one slice.
   int num_splits;
   int split_tiles;
+  int units_per_bh;
   float *o_part;
   float *lse_part;
 };
@@ -190,7 +196,13 @@ __host__ __device__ __forceinline__ int kv_tiles(const FwdParams &p, bool causal
   const int nkv = (p.Nk + 127) / 128;
   if (!causal) return nkv;
   const int last_row = min(mb * 256 + t * 128 + 127, p.N - 1);
-  return last_row / 128 + 1;
+  return min((last_row + p.q_off) / 128 + 1, nkv);
+}
+
+// Causal split: key ranges of query block mb.
+__host__ __device__ __forceinline__ int causal_ranges(const FwdParams &p, int mb) {
+  const int v0 = kv_tiles(p, true, mb, 0);
+  return max(1, (v0 + p.split_tiles - 1) / p.split_tiles);
 }
 
 // The uc-th work unit of this CTA, or -1 when none is left.
@@ -212,7 +224,26 @@ __device__ __forceinline__ int unit_at(const SchedFor<kCausal> &tab, const FwdPa
 template <bool kCausal, bool kSplit>
 __device__ __forceinline__ void unit_info(const FwdParams &p, int u, int &bh, int &mb, int &s,
                                           int &j0, int &n0, int &n1) {
-  if constexpr (kSplit) {
+  if constexpr (kSplit && kCausal) {
+    // blocks have different range counts: walk them
+    bh = u / p.units_per_bh;
+    int r = u - bh * p.units_per_bh;
+    int ranges = 1;
+    for (mb = 0; mb < p.num_mblocks - 1; ++mb) {
+      ranges = causal_ranges(p, mb);
+      if (r < ranges) break;
+      r -= ranges;
+    }
+    if (mb == p.num_mblocks - 1) ranges = causal_ranges(p, mb);
+    s = r;
+    j0 = s * p.split_tiles;
+    if (s == ranges - 1) {  // the last range: up to each tile's last visible key
+      n0 = kv_tiles(p, true, mb, 0) - j0;
+      n1 = kv_tiles(p, true, mb, 1) - j0;
+    } else {
+      n0 = n1 = p.split_tiles;
+    }
+  } else if constexpr (kSplit) {
     const int per_bh = p.num_mblocks * p.num_splits;
     bh = u / per_bh;
     const int r = u - bh * per_bh;
@@ -355,10 +386,11 @@ __global__ void __launch_bounds__(512, 1)
         }
         // Mask keys beyond N, and keys after the query under the causal mask.
         const int k0 = (j0 + j) * 128;
-        const bool need_mask = (k0 + 128 > p.Nk) || (kCausal && k0 + 127 > mb * 256 + t * 128);
+        const bool need_mask =
+            (k0 + 128 > p.Nk) || (kCausal && k0 + 127 > mb * 256 + t * 128 + p.q_off);
         if (need_mask) {
           int lim = p.Nk - k0;
-          if (kCausal) lim = min(lim, qrow - k0 + 1);
+          if (kCausal) lim = min(lim, qrow + p.q_off - k0 + 1);
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (i >= lim) s[i] = __float_as_uint(-INFINITY);
@@ -382,14 +414,18 @@ __global__ void __launch_bounds__(512, 1)
         const float m_new = grow ? m_cand : m_run;
         const float fac = grow ? ex2_approx(m_run - m_new) : 1.0f;  // 0 on the first tile
         m_run = m_new;
+        // A causal key range can hold no key visible to a row yet (its first
+        // tiles lie past the row): keep its P at 0 instead of 2^(-inf + inf).
+        float m_use = m_run;
+        if constexpr (kSplit && kCausal) m_use = m_run == -INFINITY ? 0.f : m_run;
         // The tile's largest P exactly as the loop below computes it, and the
         // error its fp16 rounding puts into the P V product.
-        const float p_max = ex2_approx(fmaf(s_max, c, -m_run));
+        const float p_max = ex2_approx(fmaf(s_max, c, -m_use));
         const float p_max_err = round_to_f16(p_max) - p_max;
         // P = 2^(s*c - m_run) <= 2^kTau, rounded to fp16 for the P V MMA;
         // the row sum is taken over the fp32 P.
         const uint64_t c2 = f2_pack(c, c);
-        const uint64_t nm2 = f2_pack(-m_run, -m_run);
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
         uint64_t la = 0, lb = 0;  // (+0.f, +0.f) pairs
         // Split P: the two tiles' softmax warps of an SM sub-partition take
         // turns at the exponentials (the special-function unit is the shared
@@ -528,7 +564,8 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after_sync();
             const float m = sb.m_fin[pend_uc & 1][t][row];
             const float l = sb.l_fin[pend_uc & 1][t][row];
-            const float oscale = exp2i(-pend_e[t]) / (l + sb.lc_fin[pend_uc & 1][t][row]);
+            float oscale = exp2i(-pend_e[t]) / (l + sb.lc_fin[pend_uc & 1][t][row]);
+            if constexpr (kSplit && kCausal) oscale = l > 0.f ? oscale : 0.f;  // no key in range
             const int qrow = pend_mb * 256 + t * 128 + row;
             const bool valid = qrow < p.N;
             const uint32_t tO = tmem + lane_off + (t ? C::kColO1 : C::kColO0);

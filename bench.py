@@ -51,10 +51,12 @@ DEFAULT_WORKLOAD = "n16384_d128_c"
 # timed beside the default workload in every run, each with its own clock record
 COMPANION_WORKLOADS = ("n4096_d128", "n8192_d128_c", "n1024_d64")
 L2_FLUSH_BYTES = 256 << 20
-# Device code of the forward kernel: recorded DRAM traffic is valid while
-# these files are unchanged.
+# Device code of the forward kernel and its host launcher (the unit order
+# decides L2 reuse): recorded DRAM traffic is valid while these files are
+# unchanged.
 KERNEL_SOURCES = ("attention_forward_tk_gb300/csrc/tk_attn_fwd.cuh",
-                  "attention_forward_tk_gb300/csrc/sm103_ptx.cuh")
+                  "attention_forward_tk_gb300/csrc/sm103_ptx.cuh",
+                  "attention_forward_tk_gb300/csrc/tk_attn.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_NAME = "tk_attn_fwd_kernel"
 

@@ -1,9 +1,9 @@
 /*
  * tk_attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
  *
- * Entry points: tk_attn_fwd (the forward pass, below), tk_attn_fwd_splitkv
- * and tk_attn_fwd_splitkv_static (queries against a longer key set, keys
- * split into ranges), tk_attn_bwd (dQ, dK, dV), tk_based_fwd (Based linear
+ * Entry points: tk_attn_fwd (the forward pass, below), tk_attn_fwd_splitkv,
+ * tk_attn_fwd_qk and tk_attn_fwd_splitkv_static (queries against a longer
+ * key set, keys split into ranges; tk_attn_fwd_qk also causal), tk_attn_bwd (dQ, dK, dV), tk_based_fwd (Based linear
  * attention) and tk_gemm_bf16 (C = A B^T), each with argument checks that
  * need no GPU, plus status, version and device-error queries.
  *
@@ -151,6 +151,30 @@ int tk_attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, fl
  * ranges, 0 for one range or for invalid sizes.
  */
 size_t tk_attn_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int D, int num_splits);
+
+/*
+ * tk_attn_fwd_qk -- tk_attn_fwd_splitkv with an optional causal mask aligned
+ * to the end of the key sequence: the Nq queries are the last Nq positions
+ * of a sequence of Nk (a prefill chunk, or a decode step, against the keys
+ * cached before it), so key j is visible to query i iff j <= i + (Nk - Nq).
+ * For Nq == Nk this is tk_attn_fwd's causal mask.
+ *
+ * Definition: the attention of the flash-attention examples in the
+ * ThunderKittens news write-up (88811315.cn, post 77732); neither those
+ * examples nor the rest of the pages fix how a causal mask aligns when
+ * queries and keys differ in number, and this is the reading where the
+ * queries come last.  causal = 0 is exactly tk_attn_fwd_splitkv.
+ *
+ * Arguments as for tk_attn_fwd_splitkv, plus causal (0 or nonzero); causal
+ * requires Nq <= Nk (else TK_ATTN_ERR_INVALID_ARG).  Under the mask each
+ * 256-query block splits only the keys it sees, into ranges of the same
+ * length as the unmasked call would use; the workspace the unmasked call
+ * needs (tk_attn_splitkv_workspace_bytes) is always enough.  Returns and
+ * errors as for tk_attn_fwd_splitkv; outputs untouched on any error.
+ */
+int tk_attn_fwd_qk(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                   int H, int Nq, int Nk, int D, float scale, int causal, int num_splits,
+                   void *workspace, size_t workspace_bytes, tk_attn_stream_t stream);
 
 /*
  * tk_attn_fwd_splitkv_static -- tk_attn_fwd_splitkv for callers that cannot

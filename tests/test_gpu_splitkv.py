@@ -109,3 +109,69 @@ def test_inference_workload_sampled_rows(tk_lib, oracle_lib):
     assert np.abs(of - o_ref).max() <= TOL_O_MAX
     assert np.abs(of - o_ref).mean() <= TOL_O_MEAN
     assert np.abs(lf - lse_ref).max() <= TOL_LSE_MAX
+
+
+def run_qk(tk_lib, q, k, v, scale, causal, splits):
+    """tk_attn_fwd_qk (optionally causal, aligned to the last key)."""
+    dev = torch.device("cuda", 0)
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device=dev)
+    need = tk_lib.tk_attn_splitkv_workspace_bytes(B, H, Nq, Nk, D, splits)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = tk_lib.tk_attn_fwd_qk(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, Nq, Nk, D, scale, int(causal), splits,
+                               ws.data_ptr(), need, stream)
+    if st == 0:
+        assert tk_lib.tk_attn_last_device_error(stream) == 0
+    torch.cuda.synchronize()
+    return st, o.float().cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+CAUSAL_CASES = [
+    # (B, H, Nq, Nk, D, splits): causal, queries are the last Nq positions
+    (1, 4, 256, 4096, 128, 0),   # a prefill chunk at the end of 4096 keys, default split
+    (2, 3, 100, 3000, 64, 5),    # ragged tails
+    (1, 8, 1, 2048, 128, 0),     # decode: one query sees every key
+    (1, 2, 300, 1000, 64, 1),    # one range: the single-pass kernel with an offset mask
+    (1, 1, 17, 129, 128, 7),
+    (1, 2, 640, 5000, 128, 3),   # blocks with different range counts
+    (1, 2, 1000, 1000, 128, 4),  # Nq == Nk: tk_attn_fwd's causal mask, split over keys
+    (1, 2, 256, 320, 128, 3),    # the first rows see no key of the last range
+    (2, 1, 256, 320, 64, 3),
+    (1, 3, 513, 2100, 64, 0),
+]
+
+
+@pytest.mark.parametrize("case", CAUSAL_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_qk_causal_parity(tk_lib, oracle_lib, case):
+    B, H, Nq, Nk, D, splits = case
+    q, k, v = draw_qk(B, H, Nq, Nk, D, seed=800 + Nq + Nk + D + splits)
+    scale = 1 / math.sqrt(D)
+    st, o, lse = run_qk(tk_lib, q, k, v, scale, True, splits)
+    assert st == 0, tk_lib.tk_attn_status_string(st)
+    o_ref, lse_ref = oracle_lib.attention_qk(q, k, v, scale, True)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    do = np.abs(o - o_ref)
+    assert do.max() <= TOL_O_MAX, do.max()
+    assert do.mean() <= TOL_O_MEAN, do.mean()
+    assert np.abs(lse - lse_ref).max() <= TOL_LSE_MAX
+
+
+def test_qk_unmasked_is_the_split_call(tk_lib):
+    # causal = 0 is tk_attn_fwd_splitkv exactly
+    q, k, v = draw_qk(1, 2, 300, 2000, 128, seed=901)
+    st1, o1, l1 = run_qk(tk_lib, q, k, v, 0.09, False, 3)
+    st2, o2, l2, _ = run_split(tk_lib, q, k, v, 0.09, 3)
+    assert st1 == 0 and st2 == 0
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_qk_causal_rejects_more_queries_than_keys(tk_lib):
+    q, k, v = draw_qk(1, 1, 300, 200, 64, seed=902)
+    st, o, lse = run_qk(tk_lib, q, k, v, 0.125, True, 0)
+    assert st == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert np.isnan(o).all() and np.isnan(lse).all()  # outputs untouched
