@@ -702,6 +702,12 @@ extern "C" int tk_attn_bwd(const void *q, const void *k, const void *v, const vo
   p.BH = BH;
   p.N = N;
   p.num_units = 0;
+  {  // causal sections: the streamed tiles of a slice (Q and dO, or K and V) take 4*N*D bytes
+    long long g = (40LL << 20) / (4LL * N * D);
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    p.head_group = (int)g;
+  }
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -44,6 +44,7 @@ struct BwdParams {
   int *err;                     // device error word
   int BH, N, Npad, nt;          // nt = Npad / 128 tiles per slice
   int num_units;
+  int head_group;               // causal order: slices per L2-sized section
   float scale, scale_log2;      // scale and scale * log2(e)
 };
 
@@ -157,13 +158,25 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
 // Units.  dkdv: u -> (slice, key tile j); non-causal slice-major (a slice's
 // key tiles share its Q/dO in L2), causal longest first (j ascending: tile j
 // meets nt - j query tiles).  dq: u -> (slice, query tile i); causal longest
-// first (i descending: tile i meets i + 1 key tiles).
+// first (i descending: tile i meets i + 1 key tiles).  Causal units go in
+// sections of head_group slices whose streamed tiles (Q and dO, or K and V)
+// fit in about 40 MB of L2, longest first within a section, so the CTAs
+// running at one time share those tiles in L2 instead of each streaming
+// another slice's from HBM.
+__device__ __forceinline__ void causal_section(const BwdParams &p, int u, int &bh, int &r) {
+  const int per_section = p.head_group * p.nt;
+  const int section = u / per_section;
+  const int rr = u - section * per_section;
+  const int g = min(p.head_group, p.BH - section * p.head_group);  // slices in this section
+  r = rr / g;  // rank by length within the section
+  bh = section * p.head_group + rr % g;
+}
+
 template <bool kCausal>
 __device__ __forceinline__ void dkdv_unit(const BwdParams &p, int u, int &bh, int &j, int &i0,
                                           int &n) {
   if (kCausal) {
-    j = u / p.BH;
-    bh = u - j * p.BH;
+    causal_section(p, u, bh, j);
     i0 = j;
     n = p.nt - j;
   } else {
@@ -177,8 +190,8 @@ __device__ __forceinline__ void dkdv_unit(const BwdParams &p, int u, int &bh, in
 template <bool kCausal>
 __device__ __forceinline__ void dq_unit(const BwdParams &p, int u, int &bh, int &i, int &n) {
   if (kCausal) {
-    const int r = u / p.BH;
-    bh = u - r * p.BH;
+    int r;
+    causal_section(p, u, bh, r);
     i = p.nt - 1 - r;
     n = i + 1;
   } else {
