@@ -14,10 +14,13 @@ Workloads (the five problem shapes the library is measured and checked on):
   n16384_d128_c   4   32  16384  128  causal   Q, K ~ 4 N(0, 1);
                                                V ~ Student-t(3), clipped to +-8
 
-and one inference shape, queries and keys of different lengths (timed beside
-them, split over keys):
+and three inference shapes, queries and keys of different lengths (timed
+beside them, split over keys):
 
-  prefill_q256_k32k_d128  B 1, H 32, Nq 256, Nk 32768, D 128, unmasked, N(0, 1)
+  prefill_q256_k32k_d128   B 1, H 32, Nq 256, Nk 32768, D 128, unmasked, N(0, 1)
+  chunk_q1024_k16k_d128_c  B 1, H 32, Nq 1024, Nk 16384, D 128, causal (the queries
+                           are the last 1024 positions), N(0, 1), seed 9
+  decode_b8_q1_k16k_d128   B 8, H 32, Nq 1, Nk 16384, D 128, unmasked, N(0, 1), seed 10
 
 the backward pass (tk_attn_bwd) on the shapes of n4096_d128 and n8192_d128_c,
 with the output gradient dO ~ N(0, 1) drawn after Q, K, V by draw_grad(),
@@ -57,7 +60,7 @@ class Workload:
     causal: bool
     dist: str  # "normal" or "peaky_t3"
     seed: int
-    Nk: int = 0  # keys per slice when it differs from N (inference shape, unmasked)
+    Nk: int = 0  # keys per slice when it differs from N (inference shapes)
 
     @property
     def keys(self) -> int:
@@ -77,10 +80,14 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """4*B*H*N*Nk*D (Nk = N but for the inference shape), halved under the
-        causal mask."""
-        f = 4.0 * self.B * self.H * self.N * self.keys * self.D
-        return f / 2 if self.causal else f
+        """4*B*H*D times the (query, key) pairs: N*Nk unmasked; under the causal
+        mask N^2/2 when Nk = N (the metric's halving), and the visible pairs
+        Nq*Nk - Nq*(Nq-1)/2 when the Nq queries are the last positions of Nk."""
+        if self.causal and self.Nk:
+            pairs = self.N * self.Nk - self.N * (self.N - 1) / 2
+        else:
+            pairs = self.N * self.keys / (2 if self.causal else 1)
+        return 4.0 * self.B * self.H * self.D * pairs
 
     @property
     def io_bytes(self) -> int:
@@ -97,11 +104,15 @@ WORKLOADS = (
     Workload("n8192_d128_c", 8, 16, 8192, 128, True, "normal", 3),
     Workload("n16384_d128_c", 4, 32, 16384, 128, True, "peaky_t3", 4),
 )
-# The inference shape (a split over keys, tk_attn_fwd_splitkv): a 256-query
-# prefill chunk of 32 heads against 32768 cached keys, unmasked.  Not one of
-# the five measured configurations; timed beside them.
+# Inference shapes (tk_attn_fwd_qk, split over keys): queries against a
+# longer run of cached keys.  Not among the five measured configurations;
+# timed beside them (bench.py --all-workloads).
 EXTRA_WORKLOADS = (
     Workload("prefill_q256_k32k_d128", 1, 32, 256, 128, False, "normal", 5, Nk=32768),
+    # a causal prefill chunk: the last 1024 positions of a 16384-token sequence
+    Workload("chunk_q1024_k16k_d128_c", 1, 32, 1024, 128, True, "normal", 9, Nk=16384),
+    # a decode step: one query per sequence against 16384 cached keys, 8 sequences
+    Workload("decode_b8_q1_k16k_d128", 8, 32, 1, 128, False, "normal", 10, Nk=16384),
 )
 BY_NAME = {w.name: w for w in WORKLOADS + EXTRA_WORKLOADS}
 

@@ -270,8 +270,8 @@ def time_gpu(w, steps: int, warmup: int, device):
         need = api.tk_attn_splitkv_workspace_bytes(w.B, w.H, w.N, w.Nk, w.D, 0)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                w.B, w.H, w.N, w.Nk, w.D, w.scale, 0, ws.data_ptr(), need, sh)
-        call = api.tk_attn_fwd_splitkv
+                w.B, w.H, w.N, w.Nk, w.D, w.scale, int(w.causal), 0, ws.data_ptr(), need, sh)
+        call = api.tk_attn_fwd_qk
         per_call = 2 if need > 0 else 1  # the ranges kernel, then the combine kernel
     else:
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
@@ -457,7 +457,7 @@ def time_e2e(w, steps: int, warmup: int, device):
             qd.copy_(q, non_blocking=True)
             kd.copy_(k, non_blocking=True)
             vd.copy_(v, non_blocking=True)
-            attention_forward_splitkv(qd, kd, vd, w.scale, 0, od, ld, ws)
+            attention_forward_splitkv(qd, kd, vd, w.scale, 0, od, ld, ws, causal=w.causal)
             o.copy_(od, non_blocking=True)
             lse.copy_(ld, non_blocking=True)
             torch.cuda.current_stream(device).synchronize()
@@ -600,6 +600,7 @@ def main():
             m = statistics.median(oms)
             c = oclk.summary()
             extra[ow.name] = {"ms": round(m, 4), "tflops": round(ow.flops / m / 1e9, 1),
+                              "hbm_gbs": round(ow.io_bytes / m / 1e6, 1),
                               "launches": n, "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
         for bw in BWD_WORKLOADS:
             with ClockSampler(device.index if world == 1 else local) as oclk:
