@@ -57,9 +57,9 @@ std::atomic<int> g_test_drop_load{0};
 std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 
-template <int D, bool kCausal, bool kSplit = false>
+template <int D, bool kCausal, bool kSplit = false, bool kHalf = false>
 int configure_kernel() {
-  auto kern = tk_attn_fwd_kernel<D, kCausal, kSplit>;
+  auto kern = tk_attn_fwd_kernel<D, kCausal, kSplit, kHalf>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            FwdCfg<D>::kSmemAlloc) != cudaSuccess)
     return TK_ATTN_ERR_LAUNCH;
@@ -104,6 +104,15 @@ void init_device(int dev, DeviceState &ds) {
   if (!st) st = configure_kernel<128, false, true>();
   if (!st) st = configure_kernel<64, true, true>();
   if (!st) st = configure_kernel<128, true, true>();
+  // launches of at most 128 queries
+  if (!st) st = configure_kernel<64, false, false, true>();
+  if (!st) st = configure_kernel<64, true, false, true>();
+  if (!st) st = configure_kernel<128, false, false, true>();
+  if (!st) st = configure_kernel<128, true, false, true>();
+  if (!st) st = configure_kernel<64, false, true, true>();
+  if (!st) st = configure_kernel<64, true, true, true>();
+  if (!st) st = configure_kernel<128, false, true, true>();
+  if (!st) st = configure_kernel<128, true, true, true>();
   if (!st && (cudaFuncSetAttribute(tk_based_fwd_kernel<false>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    BasedCfg::kSmemAlloc) != cudaSuccess ||
@@ -270,7 +279,7 @@ std::shared_ptr<SchedTable> sched_for(const FwdParams &p, int grid) {
   return tab;
 }
 
-template <int D, bool kCausal, bool kSplit = false>
+template <int D, bool kCausal, bool kSplit, bool kHalf>
 cudaError_t launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                    const FwdParams &p, int grid, cudaStream_t stream) {
   SchedFor<kCausal> tab;
@@ -281,9 +290,30 @@ cudaError_t launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorM
   } else if constexpr (kCausal) {
     tab.n = 0;  // causal key ranges run in stride order
   }
-  tk_attn_fwd_kernel<D, kCausal, kSplit>
+  tk_attn_fwd_kernel<D, kCausal, kSplit, kHalf>
       <<<grid, FwdCfg<D>::kThreads, FwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p, tab);
   return cudaGetLastError();
+}
+
+// The kernel variant for a head dim, mask and query count: with at most 128
+// queries (p.N <= 128) every unit's second Q tile is empty, and the kHalf
+// variant gives tile 0 the decoupled S and P.
+template <bool kSplit>
+cudaError_t launch_fwd(int D, bool causal, const CUtensorMap &tq, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const FwdParams &p, int grid, cudaStream_t s) {
+  const bool half = p.N <= 128;
+  if (D == 64) {
+    if (causal)
+      return half ? launch<64, true, kSplit, true>(tq, tk, tv, p, grid, s)
+                  : launch<64, true, kSplit, false>(tq, tk, tv, p, grid, s);
+    return half ? launch<64, false, kSplit, true>(tq, tk, tv, p, grid, s)
+                : launch<64, false, kSplit, false>(tq, tk, tv, p, grid, s);
+  }
+  if (causal)
+    return half ? launch<128, true, kSplit, true>(tq, tk, tv, p, grid, s)
+                : launch<128, true, kSplit, false>(tq, tk, tv, p, grid, s);
+  return half ? launch<128, false, kSplit, true>(tq, tk, tv, p, grid, s)
+              : launch<128, false, kSplit, false>(tq, tk, tv, p, grid, s);
 }
 
 }  // namespace
@@ -362,12 +392,7 @@ extern "C" int tk_attn_fwd(const void *q, const void *k, const void *v, void *o,
   }
   const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (D == 64)
-    e = causal ? launch<64, true>(tq, tk, tv, p, grid, s) : launch<64, false>(tq, tk, tv, p, grid, s);
-  else
-    e = causal ? launch<128, true>(tq, tk, tv, p, grid, s)
-               : launch<128, false>(tq, tk, tv, p, grid, s);
+  const cudaError_t e = launch_fwd<false>(D, causal != 0, tq, tk, tv, p, grid, s);
   return e == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 
@@ -530,18 +555,9 @@ int fwd_qk(const void *q, const void *k, const void *v, void *o, float *lse, int
   const int grid = p.num_units < ds->num_sms ? p.num_units : ds->num_sms;
   cudaError_t e;
   if (S == 1) {  // one range: the single-pass kernel writes O and LSE directly
-    if (D == 64)
-      e = causal ? launch<64, true>(tq, tk, tv, p, grid, s) : launch<64, false>(tq, tk, tv, p, grid, s);
-    else
-      e = causal ? launch<128, true>(tq, tk, tv, p, grid, s)
-                 : launch<128, false>(tq, tk, tv, p, grid, s);
+    e = launch_fwd<false>(D, causal != 0, tq, tk, tv, p, grid, s);
   } else {
-    if (D == 64)
-      e = causal ? launch<64, true, true>(tq, tk, tv, p, grid, s)
-                 : launch<64, false, true>(tq, tk, tv, p, grid, s);
-    else
-      e = causal ? launch<128, true, true>(tq, tk, tv, p, grid, s)
-                 : launch<128, false, true>(tq, tk, tv, p, grid, s);
+    e = launch_fwd<true>(D, causal != 0, tq, tk, tv, p, grid, s);
     if (e == cudaSuccess) {
       CombineParams cp;
       cp.S = S_layout;

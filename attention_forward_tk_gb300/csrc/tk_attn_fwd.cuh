@@ -110,7 +110,7 @@ struct NoSchedTable {};
 template <bool kCausal>
 using SchedFor = typename std::conditional<kCausal, SchedTable, NoSchedTable>::type;
 
-template <int D>
+template <int D, bool kHalf = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int kBM = 128;                  // query rows per Q tile
@@ -130,9 +130,13 @@ struct FwdCfg {
   // With D = 64 the tensor memory has room for P next to S (columns
   // [384, 512)), so the next S MMA of a tile needs only the softmax to have
   // read S, not its whole pass: S and P are decoupled.  With D = 128 the 512
-  // columns hold S and O alone and P overwrites S.
-  static constexpr bool kSplitP = D == 64;
-  static constexpr uint32_t kColP0 = kSplitP ? 384 : kColS0, kColP1 = kSplitP ? 448 : kColS1;
+  // columns hold S and O alone and P overwrites S, except in launches of at
+  // most 128 queries (kHalf): there every unit's second Q tile lies past the
+  // last query and only keeps the barrier protocol, and tile 0's P takes the
+  // second tile's S columns.
+  static constexpr bool kSplitP = D == 64 || kHalf;
+  static constexpr uint32_t kColP0 = !kSplitP ? kColS0 : D == 64 ? 384 : kColS1;
+  static constexpr uint32_t kColP1 = !kSplitP ? kColS1 : D == 64 ? 448 : kColS1 + 64;
   // converter: 16-byte words of one V tile per converter thread
   static constexpr int kConvVec = kTileBytes / 16 / 128;
   static_assert(kStages % 2 == 0, "K tiles in even stages, V tiles in odd stages");
@@ -280,13 +284,13 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo
   for (int kk = 1; kk < 8; ++kk) umma_ts_w<1>(tO, tP + kk * 8, v_lo + kk * (2048 >> 4), dhi, idO);
 }
 
-template <int D, bool kCausal, bool kSplit>
+template <int D, bool kCausal, bool kSplit, bool kHalf>
 __global__ void __launch_bounds__(512, 1)
     tk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const FwdParams p,
                        const __grid_constant__ SchedFor<kCausal> tab) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, kHalf>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdShared sb;
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(512, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sb.q_full[0][t], 1);
       mbar_init(&sb.q_full[1][t], 1);
-      mbar_init(&sb.q_empty[t], C::kSplitP ? 2 : 1);
+      mbar_init(&sb.q_empty[t], C::kSplitP && !kHalf ? 2 : 1);  // one commit per issuer
       mbar_init(&sb.s_full[t], 1);
       mbar_init(&sb.s_free[t], 4);
       mbar_init(&sb.pv_done[t], 1);
@@ -316,7 +320,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sb.kv_full[s], 1);
-      mbar_init(&sb.kv_empty[s], C::kSplitP ? 2 : 1);
+      mbar_init(&sb.kv_empty[s], C::kSplitP && !kHalf ? 2 : 1);
       mbar_init(&sb.v_ready[s], 4);
     }
     mbar_init(&sb.conv_bar, 4);
@@ -360,6 +364,10 @@ __global__ void __launch_bounds__(512, 1)
       unit_info<kCausal, kSplit>(p, u, bh, mb, sp, j0, n0, n1);
       const int n_t = t ? n1 : n0;
       const int qrow = mb * 256 + t * 128 + row;  // global query index
+      // With at most 128 queries, tile 1 and the warps of tile 0 whose 32 rows
+      // all lie past the last query keep the barrier protocol and skip the
+      // arithmetic; the two tiles then take no exponential turns.
+      const bool idle = kHalf && (t == 1 || (warp & 3) * 32 >= p.N);
       float m_run = -INFINITY, l_run = 0.f;
       float lc_run = 0.f;  // sum of (fp16(P) - P) over each tile's largest P
       int e_cur = 0;  // V exponent O is accumulated at
@@ -369,6 +377,22 @@ __global__ void __launch_bounds__(512, 1)
           goto done;
         }
         s_phase ^= 1;
+        if (idle) {
+          // split P here: S read, previous P V done, P written
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sb.s_free[t]);
+          if (steps > 0 && !mbar_wait(&sb.pv_done[t], (steps - 1) & 1, abort_flag)) {
+            raise_abort(sb, p.err, kDevErrTimeout);
+            goto done;
+          }
+          ++steps;
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sb.p_full[t]);
+            if (j == n_t - 1) mbar_arrive(&sb.fin_full[uc & 1][t]);
+          }
+          continue;
+        }
         tc_fence_after_sync();
         uint32_t s[128];
         tmem_ld_32x32b_x32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
@@ -432,7 +456,7 @@ __global__ void __launch_bounds__(512, 1)
         // bottleneck), so each one's other work overlaps the other's
         // exponentials.  Turns pair step j of tile 0 with step j of tile 1;
         // a causal unit's last tile-1 step has no partner and takes no turn.
-        const bool take_turn = C::kSplitP && (t == 0 || j < n0);
+        const bool take_turn = C::kSplitP && !kHalf && (t == 0 || j < n0);
         if (take_turn && !mbar_wait(&sb.exp_turn[t], turns & 1, abort_flag)) {
           raise_abort(sb, p.err, kDevErrTimeout);
           goto done;
@@ -750,6 +774,12 @@ __global__ void __launch_bounds__(512, 1)
           unit_info<kCausal, kSplit>(p, u, bh, mb, sp, j0, n0, n1);
           const int n_t = t ? n1 : n0;
           const int qb = uc % C::kQBufs;  // Q buffer of this unit
+          // With at most 128 queries tile 1 has no row: its thread issues no
+          // MMA and keeps only its own tile's barriers.  It neither waits for
+          // nor releases K/V stages and Q tiles (tile 0's commits alone do):
+          // a releaser that issues nothing could run a whole ring ahead and
+          // complete a stage's release while tile 0 still reads it.
+          const bool idle = kHalf && t == 1;
 #pragma unroll 1
           for (int j = 0; j <= n1; ++j) {
             const uint32_t kidx = kvb + 2 * j, vidx = kidx - 1;  // K_j and V_{j-1}
@@ -758,16 +788,18 @@ __global__ void __launch_bounds__(512, 1)
             if (do_s) {
               // S_t = Q_t K_j^T once K_j has landed and the softmax has read
               // the previous S_t
-              if (!mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag) ||
-                  (j == 0 && !mbar_wait(&sb.q_full[qb][t], (uc / C::kQBufs) & 1, abort_flag)) ||
+              if ((!idle && !mbar_wait(&sb.kv_full[ks], (kidx / C::kStages) & 1, abort_flag)) ||
+                  (j == 0 && !idle &&
+                   !mbar_wait(&sb.q_full[qb][t], (uc / C::kQBufs) & 1, abort_flag)) ||
                   (s_cnt > 0 && !mbar_wait(&sb.s_free[t], (s_cnt - 1) & 1, abort_flag))) {
                 raise_abort(sb, p.err, kDevErrTimeout);
                 goto mma_exit_split;
               }
               ++s_cnt;
               tc_fence_after_sync();
-              issue_s<D>(tS, a_lo0 + qb * (2 * C::kTileBytes >> 4), k_lo0 + ks * (C::kTileBytes >> 4),
-                         dhi, idS);
+              if (!idle)
+                issue_s<D>(tS, a_lo0 + qb * (2 * C::kTileBytes >> 4),
+                           k_lo0 + ks * (C::kTileBytes >> 4), dhi, idS);
               umma_commit(&sb.s_full[t]);
             }
             if (do_pv) {
@@ -779,15 +811,18 @@ __global__ void __launch_bounds__(512, 1)
               }
               p_phase ^= 1;
               tc_fence_after_sync();
-              issue_pv(tO, tP, v_lo0 + vs * (C::kTileBytes >> 4), dhi, idO, j > 1 ? 1u : 0u);
+              if (!idle) issue_pv(tO, tP, v_lo0 + vs * (C::kTileBytes >> 4), dhi, idO, j > 1 ? 1u : 0u);
               umma_commit(&sb.pv_done[t]);
               if (j == n_t) umma_commit(&sb.o_full[t]);
             }
             // this tile is done with K_j, V_{j-1} (and, after the unit's last S,
-            // with its Q tile); every stage gets one commit from each thread
-            if (j < n1) umma_commit(&sb.kv_empty[ks]);
-            if (j >= 1) umma_commit(&sb.kv_empty[vs]);
-            if (j == n1 - 1) umma_commit(&sb.q_empty[qb]);
+            // with its Q tile); every stage gets one commit from each issuing
+            // thread
+            if (!idle) {
+              if (j < n1) umma_commit(&sb.kv_empty[ks]);
+              if (j >= 1) umma_commit(&sb.kv_empty[vs]);
+              if (j == n1 - 1) umma_commit(&sb.q_empty[qb]);
+            }
           }
           kvb += 2 * n1;
         }

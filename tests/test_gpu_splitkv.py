@@ -51,6 +51,12 @@ CASES = [
     (1, 1, 17, 129, 128, 7),     # 2 key tiles: clamped to 2 ranges
     (2, 2, 512, 256, 64, 0),     # more queries than keys
     (1, 2, 640, 5000, 128, 3),   # 3 query blocks x 3 ranges
+    # at most 128 queries: the second Q tile of every unit is empty
+    (1, 8, 1, 2048, 64, 1),      # decode, single pass, head dim 64
+    (2, 4, 64, 1500, 128, 1),    # half of tile 0's warps hold no query
+    (1, 2, 128, 777, 64, 2),     # tile 0 full, tile 1 empty, split
+    (8, 32, 1, 4096, 128, 4),    # decode, several units per CTA (stage reuse across units)
+    (8, 32, 3, 4096, 64, 8),
 ]
 
 
@@ -111,6 +117,23 @@ def test_inference_workload_sampled_rows(tk_lib, oracle_lib):
     assert np.abs(lf - lse_ref).max() <= TOL_LSE_MAX
 
 
+@pytest.mark.parametrize("name", ["chunk_q1024_k16k_d128_c", "decode_b8_q1_k16k_d128"])
+def test_inference_workload_all_rows(tk_lib, oracle_lib, name):
+    # the other two timed inference shapes at full size, the default split
+    # count, every row against the oracle
+    from attention_forward_tk_gb300.inputs import BY_NAME, workload_inputs
+    w = BY_NAME[name]
+    q, k, v = workload_inputs(w)
+    st, o, lse = run_qk(tk_lib, q, k, v, w.scale, w.causal, 0)
+    assert st == 0, tk_lib.tk_attn_status_string(st)
+    o_ref, lse_ref = oracle_lib.attention_qk(q, k, v, w.scale, w.causal)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    do = np.abs(o - o_ref)
+    assert do.max() <= TOL_O_MAX, do.max()
+    assert do.mean() <= TOL_O_MEAN, do.mean()
+    assert np.abs(lse - lse_ref).max() <= TOL_LSE_MAX
+
+
 def run_qk(tk_lib, q, k, v, scale, causal, splits):
     """tk_attn_fwd_qk (optionally causal, aligned to the last key)."""
     dev = torch.device("cuda", 0)
@@ -143,6 +166,10 @@ CAUSAL_CASES = [
     (1, 2, 256, 320, 128, 3),    # the first rows see no key of the last range
     (2, 1, 256, 320, 64, 3),
     (1, 3, 513, 2100, 64, 0),
+    (2, 4, 64, 1500, 128, 1),    # at most 128 queries, single pass
+    (1, 2, 128, 777, 64, 2),
+    (1, 4, 33, 4000, 128, 0),
+    (4, 40, 16, 3000, 128, 3),   # several units per CTA
 ]
 
 

@@ -34,7 +34,12 @@ class Barrier:
     def __init__(self, name, count=1):
         self.name, self.count, self.arrived, self.completed = name, count, 0, 0
 
-    def arrive(self):
+    def arrive(self, phase=None):
+        # an arrival tagged with the phase it belongs to must land in that
+        # phase: with several arrivers, one that runs a whole phase ahead
+        # would otherwise complete a phase the others have not finished
+        assert phase is None or phase == self.completed, (
+            f"{self.name}: an arrival for phase {phase} lands in phase {self.completed}")
         self.arrived += 1
         if self.arrived == self.count:
             self.arrived = 0
@@ -66,8 +71,8 @@ class Sim:
                        self.bars[state[n][0]].completed > state[n][1]]
             if self.pending and (not choices or self.rng.random() < 0.3):
                 self.pending.sort()
-                _, _, b = self.pending.pop(0)
-                self.bars[b].arrive()
+                _, _, b, tag = self.pending.pop(0)
+                self.bars[b].arrive(tag)
                 continue
             if not choices:
                 stuck = {n: state[n] for n in live}
@@ -97,7 +102,7 @@ class Sim:
                         state[name] = (b, k)
                         break
                 elif kind == "arrive":
-                    self.bars[op[1]].arrive()
+                    self.bars[op[1]].arrive(op[2] if len(op) > 2 else None)
                 elif kind == "check":
                     b, k = op[1], op[2]
                     assert self.bars[b].completed > k, (
@@ -109,7 +114,9 @@ class Sim:
                     res, v = op[1], op[2]
                     last, seen = self.versions.get(res, (-1, True))
                     if kind == "write":
-                        assert v == last + 1 and seen, (
+                        # versions may skip (a unit that leaves the buffer
+                        # unused); the one written before must have been read
+                        assert v > last and seen, (
                             f"{name}: writes version {v} of {res} while version {last} "
                             f"{'was' if seen else 'was not yet'} read")
                         self.versions[res] = (v, False)
@@ -118,11 +125,13 @@ class Sim:
                             f"{name}: reads version {v} of {res}, which holds {last}")
                         self.versions[res] = (v, True)
                 elif kind == "commit":
-                    issuer = op[2] if len(op) > 2 else name
+                    # ("commit", barrier[, issuer[, phase tag]])
+                    issuer = op[2] if len(op) > 2 and op[2] is not None else name
+                    tag = op[3] if len(op) > 3 else None
                     t = max(self.now + self.rng.randint(1, 40), self.last_ready.get(issuer, 0))
                     self.last_ready[issuer] = t
                     self.seq += 1
-                    self.pending.append((t, self.seq, op[1]))
+                    self.pending.append((t, self.seq, op[1], tag))
 
 
 def based_roles(sim, units, S=8, NB=3):
@@ -371,10 +380,23 @@ def gemm_pair_roles(sim, tiles, k_blocks, S=6):
             "epi1": epilogue(1), "rel0": release(0), "rel1": release(1)}
 
 
-def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
+def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=(), half=False,
+              idle0=False, half_shared_stages=False):
     """tk_attn_fwd_kernel (one CTA).  units = list of (n0, n1): the K/V steps
     of Q tile 0 and Q tile 1 of each unit (n1 = n0 + 1 for a causal diagonal
-    block, n0 = n1 otherwise).  split_p: head dim 64 (P in its own tensor
+    block, n0 = n1 otherwise).  half: a launch of at most 128 queries (P split
+    from S at either head dim), where tile 1 holds no query row in any unit:
+    its softmax warps and MMA thread keep the barriers of their own tile
+    (S, P, P V done, the final row statistics, O) but read no S, V or
+    statistics, and neither wait for K/V or Q tiles nor release them; the
+    stage and Q-buffer barriers take tile 0's commits alone, and no
+    exponential turns are taken.  half_shared_stages replays the first
+    version, where tile 1's thread still committed every stage release (a
+    second arrival that can run a whole phase ahead).  idle0: tile 0's warps
+    split into a working role and a role for the warps whose rows all lie
+    past the last query, which keep the protocol with no waits for V and no
+    final statistics; tile 0's 4-warp barriers then take one arrival from
+    each.  split_p: head dim 64 (P in its own tensor
     memory columns, one MMA issuer per tile, exponential turns); otherwise
     head dim 128 (P over S, one issuer for both tiles).  single_fin replays
     the earlier one-buffer fin_full, and `drop` leaves out the softmax's
@@ -385,7 +407,10 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
     role each: their 4-arrival barriers are modelled with one arrival."""
     S = S or (8 if split_p else 4)
     QB = QB or (2 if split_p else 1)
-    nissue = 2 if split_p else 1
+    nissue = 2 if split_p and (not half or half_shared_stages) else 1
+    if idle0:
+        for name in ("s_free0", "p_full0", "fin_full0_0", "fin_full1_0"):
+            sim.bar(name, 2)
     for t in range(2):
         for b in range(QB):
             sim.bar(f"q_full{b}_{t}")
@@ -400,6 +425,7 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
         sim.bar(f"kv_full{s_}"), sim.bar(f"kv_empty{s_}", nissue), sim.bar(f"v_ready{s_}")
     sim.bar("conv_bar")
     sim.bars["exp_turn0"].completed = 1  # tile 0 takes the first turn (set at start-up)
+    units = [tuple(u) + (half,) for u in units]
 
     def fin(uc, t):
         # double-buffered by unit parity; the earlier version had one buffer
@@ -407,7 +433,7 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
 
     def producer():
         kv_idx = 0
-        for uc, (n0, n1) in enumerate(units):
+        for uc, (n0, n1, _) in enumerate(units):
             qb = uc % QB
             if uc >= QB:
                 yield ("wait", f"q_empty{qb}", uc // QB - 1)
@@ -430,17 +456,18 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
             yield ("wait", f"q_full{b}_0", last // QB)
             yield ("wait", f"q_full{b}_1", last // QB)
 
-    def softmax(t):
+    def softmax(t, idle_warps=False):
         steps = turns = kvb = 0
         s_waits = 0
-        for uc, (n0, n1) in enumerate(units):
+        for uc, (n0, n1, idle1) in enumerate(units):
             n_t = n1 if t else n0
+            idle = (t == 1 and idle1) or idle_warps
             for j in range(n_t):
                 yield ("wait", f"s_full{t}", s_waits)
                 s_waits += 1
                 if split_p:
-                    yield ("arrive", f"s_free{t}")
-                take_turn = split_p and (t == 0 or j < n0)
+                    yield ("arrive", f"s_free{t}", s_waits - 1)
+                take_turn = split_p and not idle1 and (t == 0 or j < n0)
                 if take_turn:
                     yield ("wait", f"exp_turn{t}", turns)
                     turns += 1
@@ -450,14 +477,14 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
                         yield ("wait", f"pv_done{t}", steps - 1)
                     steps += 1
                 vidx = kvb + 2 * j + 1
-                if "v_ready" not in drop:
+                if "v_ready" not in drop and not idle:
                     yield ("wait", f"v_ready{vidx % S}", vidx // S)
-                if j == n_t - 1:
+                if j == n_t - 1 and not idle:
                     yield ("write", f"fin{uc & 1 if not single_fin else 0}_{t}",
                            uc >> 1 if not single_fin else uc)
-                yield ("arrive", f"p_full{t}")
+                yield ("arrive", f"p_full{t}", s_waits - 1)
                 if j == n_t - 1:
-                    yield ("arrive", fin(uc, t)[0])
+                    yield ("arrive", *fin(uc, t))
             kvb += 2 * n1
 
     def converter():
@@ -472,8 +499,9 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
                         bar, k = fin(pend, t)
                         yield ("wait", bar, k)
                         yield ("wait", f"o_full{t}", pend)
-                        yield ("read", f"fin{pend & 1 if not single_fin else 0}_{t}",
-                               pend >> 1 if not single_fin else pend)
+                        if not (t == 1 and units[pend][2]):
+                            yield ("read", f"fin{pend & 1 if not single_fin else 0}_{t}",
+                                   pend >> 1 if not single_fin else pend)
                         yield ("arrive", f"o_free{t}")
                     pend = None
                 if j == n1:
@@ -492,17 +520,20 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
 
     def mma_split(t):
         p_cnt = s_cnt = kvb = 0
-        for uc, (n0, n1) in enumerate(units):
+        for uc, (n0, n1, idle1) in enumerate(units):
             n_t = n1 if t else n0
+            idle = t == 1 and idle1
             qb = uc % QB
             for j in range(n1 + 1):
                 kidx = kvb + 2 * j
                 vidx = kidx - 1
                 ks, vs = kidx % S, vidx % S
                 do_s, do_pv = j < n_t, 1 <= j <= n_t
+                stages = not idle or half_shared_stages  # waits for and releases K/V, Q
                 if do_s:
-                    yield ("wait", f"kv_full{ks}", kidx // S)
-                    if j == 0:
+                    if stages:
+                        yield ("wait", f"kv_full{ks}", kidx // S)
+                    if j == 0 and stages:
                         yield ("wait", f"q_full{qb}_{t}", uc // QB)
                     if s_cnt > 0:
                         yield ("wait", f"s_free{t}", s_cnt - 1)
@@ -513,16 +544,17 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
                         yield ("wait", f"o_free{t}", uc - 1)
                     yield ("wait", f"p_full{t}", p_cnt)
                     p_cnt += 1
-                    yield ("check", f"v_ready{vs}", vidx // S)  # V_{j-1} converted
+                    if not idle:
+                        yield ("check", f"v_ready{vs}", vidx // S)  # V_{j-1} converted
                     yield ("commit", f"pv_done{t}")
                     if j == n_t:
                         yield ("commit", f"o_full{t}")
-                if j < n1:
-                    yield ("commit", f"kv_empty{ks}")
-                if j >= 1:
-                    yield ("commit", f"kv_empty{vs}")
-                if j == n1 - 1:
-                    yield ("commit", f"q_empty{qb}")
+                if j < n1 and stages:
+                    yield ("commit", f"kv_empty{ks}", None, kidx // S)
+                if j >= 1 and stages:
+                    yield ("commit", f"kv_empty{vs}", None, vidx // S)
+                if j == n1 - 1 and stages:
+                    yield ("commit", f"q_empty{qb}", None, uc // QB)
             kvb += 2 * n1
         yield ("commit", f"mma_done{t}")
         yield ("wait", f"mma_done{t}", 0)
@@ -530,7 +562,7 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
     def mma_shared():
         p_cnt = [0, 0]
         kvb = 0
-        for uc, (n0, n1) in enumerate(units):
+        for uc, (n0, n1, idle1) in enumerate(units):
             for j in range(n1 + 1):
                 kidx = kvb + 2 * j
                 vidx = kidx - 1
@@ -538,6 +570,7 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
                 k_ready = False
                 for t in range(2):
                     n_t = n1 if t else n0
+                    idle = t == 1 and idle1
                     do_pv, do_s = 1 <= j <= n_t, j < n_t
                     if do_pv:
                         if j == 1 and uc > 0:
@@ -550,25 +583,28 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=()):
                         if not k_ready and "k_wait" not in drop:
                             yield ("wait", f"kv_full{ks}", kidx // S)
                         k_ready = True
-                    if do_pv:
+                    if do_pv and not idle:
                         yield ("check", f"v_ready{vs}", vidx // S)  # V_{j-1} converted
                     if do_s:
-                        yield ("check", f"kv_full{ks}", kidx // S)  # K_j landed
+                        if not idle:
+                            yield ("check", f"kv_full{ks}", kidx // S)  # K_j landed
                         yield ("commit", f"s_full{t}")
                     if do_pv and j == n_t:
                         yield ("commit", f"o_full{t}")
                 if j < n1:
-                    yield ("commit", f"kv_empty{ks}")
+                    yield ("commit", f"kv_empty{ks}", None, kidx // S)
                 if j >= 1:
-                    yield ("commit", f"kv_empty{vs}")
+                    yield ("commit", f"kv_empty{vs}", None, vidx // S)
                 if j == n1 - 1:
-                    yield ("commit", "q_empty0")
+                    yield ("commit", "q_empty0", None, uc)
             kvb += 2 * n1
         yield ("commit", "mma_done0")
         yield ("wait", "mma_done0", 0)
 
     roles = {"producer": producer(), "softmax0": softmax(0), "softmax1": softmax(1),
              "converter": converter()}
+    if idle0:
+        roles["softmax0_idle"] = softmax(0, idle_warps=True)
     if split_p:
         roles["mma0"], roles["mma1"] = mma_split(0), mma_split(1)
     else:
@@ -593,6 +629,38 @@ def test_forward_protocol(split_p, units):
     for seed in range(80):
         sim = Sim(seed)
         sim.run(fwd_roles(sim, units, split_p))
+
+
+HALF_UNITS = [[(1, 1)] * 7, [(3, 3)] * 5, [(8, 8)] * 3, [(2, 2), (1, 1), (5, 5), (1, 1)]]
+
+
+@pytest.mark.parametrize("units", HALF_UNITS, ids=["1x7", "3x5", "8x3", "mixed"])
+@pytest.mark.parametrize("idle0", [False, True], ids=["tile0_full", "tile0_part"])
+def test_forward_protocol_at_most_128_queries(units, idle0):
+    """Launches of at most 128 queries: P split from S at either head dim
+    (head dim 128: four stages, one Q buffer; 64: eight and two), tile 1 idle
+    in every unit, tile 0's warps past the last query idle or not."""
+    for seed in range(150):
+        for S, QB in ((4, 1), (8, 2)):
+            sim = Sim(seed)
+            sim.run(fwd_roles(sim, units, True, S=S, QB=QB, half=True, idle0=idle0))
+
+
+def test_forward_idle_tile_stage_releases_run_ahead():
+    """The fault the single-issuer stage release fixed: when tile 1's MMA
+    thread, which issues nothing, still gave every K/V stage one of its two
+    releases, it could run a whole ring ahead and complete a stage's release
+    for a fill that tile 0's P V was still reading."""
+    failures = 0
+    for seed in range(300):
+        sim = Sim(seed)
+        try:
+            sim.run(fwd_roles(sim, [(8, 8)] * 3, True, S=4, QB=1, half=True, idle0=True,
+                              half_shared_stages=True))
+        except AssertionError as e:
+            assert "lands in phase" in str(e) or "completed" in str(e), str(e)
+            failures += 1
+    assert failures > 0
 
 
 @pytest.mark.parametrize("split_p", [True, False], ids=["d64_split_p", "d128_shared_sp"])
