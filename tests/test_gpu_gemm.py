@@ -58,6 +58,7 @@ CASES = [
     (4096, 4096, 256),  # 512 tiles: several per CTA, both accumulators, ring wrap-around
     (256, 512, 8192),   # 128 K blocks through the 4-stage ring
     (130, 264, 72),     # tails of one row, 8 columns and 8 K-columns past full tiles
+    (2048, 2048, 512),  # 64 tiles: one wave more than half full, no tile split into halves
 ]
 
 
