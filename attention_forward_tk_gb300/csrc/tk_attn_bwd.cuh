@@ -59,7 +59,6 @@ struct BwdCfg {
   // dq: K and V rings of their own (K is needed one step earlier than V)
   static constexpr int kKStages = D == 128 ? 3 : 4, kVStages = D == 128 ? 2 : 4;
   static constexpr int kDqSmemAlloc = (2 + kKStages + kVStages) * kTileBytes + 1024;
-  static constexpr uint32_t kColS1 = 384;  // dq: second S buffer
   static constexpr int kDqThreads = 576;   // dq: 16 elementwise warps, producer, MMA
   static constexpr int kThreads = 320;            // 8 elementwise warps, producer, MMA
   // TMEM columns: S (or S^T), dP (or dP^T), and the D-wide accumulators
@@ -71,7 +70,7 @@ struct BwdShared {
   uint64_t fix_full, fix_empty;  // the unit's resident pair landed / released
   uint64_t ring_full[kStages], ring_empty[kStages];
   uint64_t s_full;               // S (dkdv: S^T) of a step complete   (commit)
-  uint64_t p_full;               // bf16 P (dq: dS) of a step in TMEM  (8 warps)
+  uint64_t p_full;               // bf16 P^T of a step in TMEM         (8 warps)
   uint64_t dp_full;              // dkdv: dP^T of a step complete      (commit)
   uint64_t ds_full;              // dkdv: bf16 dS^T of a step in TMEM  (8 warps)
   uint64_t acc_full, acc_empty;  // unit's accumulators done / read    (commit / 8 warps)
@@ -520,20 +519,26 @@ struct DqShared {
   uint64_t fix_full, fix_empty;  // the unit's Q_i, dO_i landed / released
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full;               // S and dP of a step complete   (commit)
-  uint64_t p_full;               // bf16 dS of a step in TMEM     (8 warps)
-  uint64_t acc_full, acc_empty;  // dQ done / read                (commit / 8 warps)
+  uint64_t s_full;               // S_j complete                          (commit)
+  uint64_t s_read;               // S_j read into registers               (16 warps)
+  uint64_t dp_full;              // dP_j complete (over S_j)              (commit)
+  uint64_t ds_full;              // bf16 dS_j in TMEM (over dP_j)         (16 warps)
+  uint64_t acc_full, acc_empty;  // dQ done / read                        (commit / 16 warps)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
 // Sixteen elementwise warps, four per TMEM lane quadrant, each on 32 of the
-// 128 key columns.  Per step j (key tile j) the MMA thread issues S_{j+1} = Q K_{j+1}^T into
-// the other S buffer before it waits for the elementwise warps' dS_j, so the
-// tensor core computes the next scores while the warps work:
-//   S_{j+1} | wait dS_j: dQ += dS_j K_j, dP_{j+1} = dO V_{j+1}^T | wait dS_{j+1}
-// dP_{j+1} overwrites dS_j only after the MMA that reads it (in-order issue).
+// 128 key columns.  Step j (key tile j) lives in one of two 128-column
+// buffers, b = j mod 2: S_j = Q K_j^T, then dP_j = dO V_j^T over it once the
+// warps hold S_j in registers, then bf16 dS_j over dP_j, which dQ += dS_j K_j
+// reads.  The MMA thread issues, per step,
+//   wait S_j read: dP_j | S_{j+1} (other buffer) | wait dS_j: dQ += dS_j K_j
+// so the tensor core computes dP_j and S_{j+1} while the warps compute P_j
+// and then dS_j, and dP_{j+1} follows dQ_j as soon as S_{j+1} has been read.
+// In-order issue keeps every buffer's products apart: S_{j+2} overwrites
+// dS_j only after the dQ product that reads it.
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(576, 1)
     tk_attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -562,7 +567,9 @@ __global__ void __launch_bounds__(576, 1)
       mbar_init(&sb.v_empty[s], 1);
     }
     mbar_init(&sb.s_full, 1);
-    mbar_init(&sb.p_full, 16);
+    mbar_init(&sb.s_read, 16);
+    mbar_init(&sb.dp_full, 1);
+    mbar_init(&sb.ds_full, 16);
     mbar_init(&sb.acc_full, 1);
     mbar_init(&sb.acc_empty, 16);
     mbar_init(&sb.mma_done, 1);
@@ -581,7 +588,7 @@ __global__ void __launch_bounds__(576, 1)
     sb.abort = 1;
     atomicCAS(p.err, 0, kDevErrTimeout);
   };
-  auto s_col = [](uint32_t step) { return (step & 1) ? C::kColS1 : C::kColS; };
+  auto s_col = [](uint32_t step) { return (step & 1) ? C::kColdP : C::kColS; };
 
   if (warp < 16) {
     // ---------------------------------------------------------- elementwise
@@ -606,21 +613,22 @@ __global__ void __launch_bounds__(576, 1)
           break;
         }
         tc_fence_after_sync();
-        const uint32_t tS = tmem + lane_off + s_col(it);
+        const uint32_t tS = tmem + lane_off + s_col(it) + 32 * h;
         const bool edge = (kCausal && j == i) || (j * 128 + 128 > p.N);
         {
           const int col0 = 32 * h;
-          uint32_t sv[32], dv[32];
-          tmem_ld_32x32b_x32(tS + col0, sv);
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
+          uint32_t sv[32];
+          tmem_ld_32x32b_x32(tS, sv);
           tmem_wait_ld();
-          uint32_t dk[16];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) reg_barrier(sv[t]);
+          // S_j is in registers: dP_j may overwrite it
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sb.s_read);
+          uint64_t pp[16];  // P in fp32 pairs, held while dP_j is computed
 #pragma unroll
           for (int t = 0; t < 32; t += 2) {
-            reg_barrier(sv[t]);
-            reg_barrier(sv[t + 1]);
-            reg_barrier(dv[t]);
-            reg_barrier(dv[t + 1]);
             float a0, a1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), c2, nl2),
                       a0, a1);
@@ -630,19 +638,35 @@ __global__ void __launch_bounds__(576, 1)
               if ((kCausal && kj > qi) || kj >= p.N) p0 = 0.f;
               if ((kCausal && kj + 1 > qi) || kj + 1 >= p.N) p1 = 0.f;
             }
+            pp[t >> 1] = f2_pack(p0, p1);
+          }
+          if (!mbar_wait(&sb.dp_full, it & 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          uint32_t dv[32];
+          tmem_ld_32x32b_x32(tS, dv);
+          tmem_wait_ld();
+          uint32_t dk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            reg_barrier(dv[t]);
+            reg_barrier(dv[t + 1]);
             float d0, d1;
-            f2_unpack(f2_mul(f2_pack(p0, p1),
+            f2_unpack(f2_mul(pp[t >> 1],
                              f2_add(f2_pack(__uint_as_float(dv[t]), __uint_as_float(dv[t + 1])),
                                     ndl)),
                       d0, d1);
             dk[t >> 1] = pack_bf16x2(d0, d1);
           }
-          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 32 * h, dk);
+          tmem_st_32x32b_x16(tS, dk);
         }
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sb.p_full);
+        if (lane == 0) mbar_arrive(&sb.ds_full);
       }
       if (!ok) break;
       // ---- epilogue: scale * dQ of this query tile, rows < N
@@ -733,29 +757,32 @@ __global__ void __launch_bounds__(576, 1)
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
       int bh, i, n;
       dq_unit<kCausal>(p, u, bh, i, n);
-      // step 0: S_0 = Q K_0^T and dP_0 = dO V_0^T (rows: queries; columns: keys)
+      // S_0 = Q K_0^T (rows: queries; columns: keys)
       if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag) ||
-          !mbar_wait(&sb.k_full[it % KS], (it / KS) & 1, abort_flag) ||
-          !mbar_wait(&sb.v_full[it % VS], (it / VS) & 1, abort_flag)) {
+          !mbar_wait(&sb.k_full[it % KS], (it / KS) & 1, abort_flag)) {
         fail();
         break;
       }
       tc_fence_after_sync();
       issue_s<D>(tmem + s_col(it), q_lo, sdesc_sw128_lo(k_addr(it), 16), dhi, idS);
-      issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(v_addr(it), 16), dhi, idS);
       umma_commit(&sb.s_full);
-      umma_commit(&sb.v_empty[it % VS]);
-      // Q_i and dO_i are read by the S and dP products only: the last dP
-      // releases them, so the next unit's pair loads during this unit's tail
-      if (n == 1) umma_commit(&sb.fix_empty);
-      if (uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) {
-        fail();
-        break;
-      }
       for (int j = 0; j < n; ++j, ++it) {
-        const bool more = j + 1 < n;
-        if (more) {
-          // the next scores, into the other S buffer, while the warps work
+        // dP_j = dO V_j^T over S_j, once the warps hold S_j
+        if (!mbar_wait(&sb.s_read, it & 1, abort_flag) ||
+            !mbar_wait(&sb.v_full[it % VS], (it / VS) & 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_s<D>(tmem + s_col(it), do_lo, sdesc_sw128_lo(v_addr(it), 16), dhi, idS);
+        umma_commit(&sb.dp_full);
+        umma_commit(&sb.v_empty[it % VS]);
+        // Q_i and dO_i are read by the S and dP products only: the last dP
+        // releases them, so the next unit's pair loads during this unit's tail
+        if (j + 1 == n) umma_commit(&sb.fix_empty);
+        if (j + 1 < n) {
+          // the next scores, into the other buffer, while the warps work
           if (!mbar_wait(&sb.k_full[(it + 1) % KS], ((it + 1) / KS) & 1, abort_flag)) {
             fail();
             ok = false;
@@ -763,29 +790,20 @@ __global__ void __launch_bounds__(576, 1)
           }
           tc_fence_after_sync();
           issue_s<D>(tmem + s_col(it + 1), q_lo, sdesc_sw128_lo(k_addr(it + 1), 16), dhi, idS);
+          umma_commit(&sb.s_full);
         }
-        if (!mbar_wait(&sb.p_full, it & 1, abort_flag)) {
+        // dQ += dS_j K_j (B operand MN-major); the unit's first one overwrites
+        // dQ, after the previous unit's epilogue has read it
+        if ((j == 0 && uc > 0 && !mbar_wait(&sb.acc_empty, (uc - 1) & 1, abort_flag)) ||
+            !mbar_wait(&sb.ds_full, it & 1, abort_flag)) {
           fail();
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        // dQ += dS K (B operand MN-major)
-        issue_grad<4>(tmem + C::kColA, tmem + C::kColdP,
+        issue_grad<4>(tmem + C::kColA, tmem + s_col(it),
                       sdesc_sw128_lo(k_addr(it), C::kChunkBytes), dhi, idG, j > 0 ? 1u : 0u);
         umma_commit(&sb.k_empty[it % KS]);
-        if (more) {
-          if (!mbar_wait(&sb.v_full[(it + 1) % VS], ((it + 1) / VS) & 1, abort_flag)) {
-            fail();
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          issue_s<D>(tmem + C::kColdP, do_lo, sdesc_sw128_lo(v_addr(it + 1), 16), dhi, idS);
-          umma_commit(&sb.s_full);
-          umma_commit(&sb.v_empty[(it + 1) % VS]);
-          if (j + 2 == n) umma_commit(&sb.fix_empty);
-        }
       }
       if (!ok) break;
       umma_commit(&sb.acc_full);

@@ -194,9 +194,14 @@ def based_roles(sim, units, S=8, NB=3):
 
 
 def dq_roles(sim, units, KS=3, VS=2):
-    """tk_attn_bwd_dq_kernel (second S buffer, separate K and V rings)."""
-    for b in ("fix_full", "fix_empty", "s_full", "p_full", "acc_full", "acc_empty"):
+    """tk_attn_bwd_dq_kernel: two 128-column buffers, step j in buffer j mod
+    2 (S_j, then dP_j over it once the warps hold S_j in registers, then bf16
+    dS_j over dP_j), separate K and V rings.  Buffer contents are versioned:
+    S_{j+2} may overwrite buffer b only after the dQ product has read dS_j,
+    and dP_j only after the warps have read S_j."""
+    for b in ("fix_full", "fix_empty", "s_full", "dp_full", "acc_full"):
         sim.bar(b)
+    sim.bar("s_read", 1), sim.bar("ds_full", 1), sim.bar("acc_empty", 1)
     for s in range(KS):
         sim.bar(f"k_full{s}"), sim.bar(f"k_empty{s}")
     for s in range(VS):
@@ -218,41 +223,48 @@ def dq_roles(sim, units, KS=3, VS=2):
                 it += 1
 
     def mma():
+        # In-order execution: a product's writes and reads take effect in
+        # issue order, so the buffer versions are advanced at issue.
         it = 0
         for uc, n in enumerate(units):
             yield ("wait", "fix_full", uc)
             yield ("wait", f"k_full{it % KS}", it // KS)
-            yield ("wait", f"v_full{it % VS}", it // VS)
-            yield ("commit", "s_full")
-            yield ("commit", f"v_empty{it % VS}")
-            if n == 1:
-                yield ("commit", "fix_empty")
-            if uc > 0:
-                yield ("wait", "acc_empty", uc - 1)
+            yield ("write", f"buf{it & 1}", 3 * it)        # S_it
+            yield ("commit", "s_full", None, it)
             for j in range(n):
-                more = j + 1 < n
-                if more:
+                yield ("wait", "s_read", it)
+                yield ("wait", f"v_full{it % VS}", it // VS)
+                yield ("write", f"buf{it & 1}", 3 * it + 1)    # dP_it over S_it
+                yield ("commit", "dp_full", None, it)
+                yield ("commit", f"v_empty{it % VS}", None, it // VS)
+                if j + 1 == n:
+                    yield ("commit", "fix_empty", None, uc)
+                if j + 1 < n:
                     yield ("wait", f"k_full{(it + 1) % KS}", (it + 1) // KS)
-                yield ("wait", "p_full", it)
-                yield ("commit", f"k_empty{it % KS}")
-                if more:
-                    yield ("wait", f"v_full{(it + 1) % VS}", (it + 1) // VS)
-                    yield ("commit", "s_full")
-                    yield ("commit", f"v_empty{(it + 1) % VS}")
-                    if j + 2 == n:
-                        yield ("commit", "fix_empty")
+                    yield ("write", f"buf{(it + 1) & 1}", 3 * (it + 1))   # S_{it+1}
+                    yield ("commit", "s_full", None, it + 1)
+                if j == 0 and uc > 0:
+                    yield ("wait", "acc_empty", uc - 1)
+                yield ("wait", "ds_full", it)
+                yield ("read", f"buf{it & 1}", 3 * it + 2)     # dS_it, by dQ += dS K
+                yield ("commit", f"k_empty{it % KS}", None, it // KS)
                 it += 1
-            yield ("commit", "acc_full")
+            yield ("commit", "acc_full", None, uc)
 
     def warps():
         it = 0
         for uc, n in enumerate(units):
             for _ in range(n):
                 yield ("wait", "s_full", it)
-                yield ("arrive", "p_full")
+                yield ("read", f"buf{it & 1}", 3 * it)
+                yield ("arrive", "s_read", it)
+                yield ("wait", "dp_full", it)
+                yield ("read", f"buf{it & 1}", 3 * it + 1)
+                yield ("write", f"buf{it & 1}", 3 * it + 2)    # dS over dP
+                yield ("arrive", "ds_full", it)
                 it += 1
             yield ("wait", "acc_full", uc)
-            yield ("arrive", "acc_empty")
+            yield ("arrive", "acc_empty", uc)
 
     return {"producer": producer(), "mma": mma(), "warps": warps()}
 
