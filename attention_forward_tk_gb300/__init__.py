@@ -32,6 +32,7 @@ from .api import (  # noqa: F401
     tk_attn_version,
     tk_based_check_args,
     tk_based_fwd,
+    tk_based_fwd_linear,
     tk_gemm_bf16,
     tk_gemm_bf16_check_args,
     version,

@@ -46,6 +46,7 @@ EXPORTED = (
     "tk_attn_bwd_workspace_bytes",
     "tk_attn_bwd_check_args",
     "tk_based_fwd",
+    "tk_based_fwd_linear",
     "tk_based_check_args",
 )
 
@@ -109,6 +110,8 @@ def library() -> ctypes.CDLL:
                                                vp, ctypes.c_size_t]
         lib.tk_based_fwd.restype = i
         lib.tk_based_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.tk_based_fwd_linear.restype = i
+        lib.tk_based_fwd_linear.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
         lib.tk_based_check_args.restype = i
         lib.tk_based_check_args.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f]
         lib.tk_gemm_bf16.restype = i
@@ -203,6 +206,12 @@ def tk_based_fwd(q: int, k: int, v: int, y: int, z: int, B: int, H: int, N: int,
                  Dv: int, scale: float, causal: int, stream: int) -> int:
     return int(library().tk_based_fwd(q, k, v, y, z, B, H, N, Df, Dv, ctypes.c_float(scale),
                                       int(causal), stream))
+
+
+def tk_based_fwd_linear(q: int, k: int, v: int, y: int, z: int, B: int, H: int, N: int,
+                        Df: int, Dv: int, scale: float, stream: int) -> int:
+    return int(library().tk_based_fwd_linear(q, k, v, y, z, B, H, N, Df, Dv,
+                                             ctypes.c_float(scale), stream))
 
 
 def tk_based_check_args(q: int, k: int, v: int, y: int, z: int, B: int, H: int, N: int, Df: int,
@@ -340,9 +349,13 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
 
 
 def based_forward(q, k, v, causal: bool = True, scale: float | None = None, out=None, z=None,
-                  stream=None):
+                  stream=None, algorithm: str = "auto"):
     """Based linear attention: y, z for bf16 CUDA tensors q, k [B, H, N, 16] and
-    v [B, H, N, 64] (scale defaults to 1/sqrt(16)).  Enqueued on `stream`."""
+    v [B, H, N, 64] (scale defaults to 1/sqrt(16)).  Enqueued on `stream`.
+
+    algorithm: "direct" (tk_based_fwd, every visible pair), "linear"
+    (tk_based_fwd_linear, chunks and a running state; causal only) or "auto"
+    (linear for causal calls longer than 256 positions, else direct)."""
     import torch
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
         raise ValueError("q, k must be [B, H, N, Df] and v [B, H, N, Dv]")
@@ -355,10 +368,21 @@ def based_forward(q, k, v, causal: bool = True, scale: float | None = None, out=
         scale = 1.0 / math.sqrt(Df)
     out = torch.empty_like(v) if out is None else out
     z = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if z is None else z
-    st = tk_based_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), z.data_ptr(),
-                      B, H, N, Df, Dv, float(scale), int(bool(causal)), _stream_handle(stream))
+    if algorithm not in ("auto", "direct", "linear"):
+        raise ValueError(f"unknown algorithm {algorithm!r}")
+    if algorithm == "linear" and not causal:
+        raise ValueError("the linear-time Based kernel is causal only")
+    if algorithm == "linear" or (algorithm == "auto" and causal and N > 256):
+        st = tk_based_fwd_linear(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 z.data_ptr(), B, H, N, Df, Dv, float(scale),
+                                 _stream_handle(stream))
+        name = "tk_based_fwd_linear"
+    else:
+        st = tk_based_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), z.data_ptr(),
+                          B, H, N, Df, Dv, float(scale), int(bool(causal)), _stream_handle(stream))
+        name = "tk_based_fwd"
     if st != TK_ATTN_OK:
-        raise TkAttnError(f"tk_based_fwd: {tk_attn_status_string(st)} ({st})", st)
+        raise TkAttnError(f"{name}: {tk_attn_status_string(st)} ({st})", st)
     return out, z
 
 

@@ -21,6 +21,7 @@
 #include "tk_attn_bwd.cuh"
 #include "tk_attn_fwd.cuh"
 #include "tk_based.cuh"
+#include "tk_based_linear.cuh"
 #include "tk_gemm.cuh"
 
 namespace tkattn {
@@ -118,7 +119,10 @@ void init_device(int dev, DeviceState &ds) {
                                    BasedCfg::kSmemAlloc) != cudaSuccess ||
               cudaFuncSetAttribute(tk_based_fwd_kernel<true>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   BasedCfg::kSmemAlloc) != cudaSuccess))
+                                   BasedCfg::kSmemAlloc) != cudaSuccess ||
+              cudaFuncSetAttribute(tk_based_linear_kernel,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   BasedLinCfg::kSmemAlloc) != cudaSuccess))
     st = TK_ATTN_ERR_LAUNCH;
   if (!st) st = configure_bwd<64, false>();
   if (!st) st = configure_bwd<64, true>();
@@ -801,6 +805,37 @@ extern "C" int tk_based_fwd(const void *q, const void *k, const void *v, void *y
   else
     tk_based_fwd_kernel<false><<<grid, BasedCfg::kThreads, BasedCfg::kSmemAlloc, s>>>(tq, tk, tv,
                                                                                      p);
+  return cudaGetLastError() == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
+}
+
+extern "C" int tk_based_fwd_linear(const void *q, const void *k, const void *v, void *y, float *z,
+                                   int B, int H, int N, int Df, int Dv, float scale,
+                                   tk_attn_stream_t stream) {
+  int st = tk_based_check_args(q, k, v, y, z, B, H, N, Df, Dv, scale);
+  if (st) return st;
+  if (!(scale >= 0.f)) return TK_ATTN_ERR_INVALID_ARG;  // the feature maps take sqrt(scale)
+  DeviceState *ds = current_device(&st);
+  if (!ds) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_feat(&tq, q, BH, N) || !make_map_feat(&tk, k, BH, N) ||
+      !make_map(&tv, v, BH, N, Dv))
+    return TK_ATTN_ERR_LAUNCH;
+  BasedLinParams p;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.k = static_cast<const __nv_bfloat16 *>(k);
+  p.y = static_cast<__nv_bfloat16 *>(y);
+  p.z = z;
+  p.err = ds->err_word;
+  p.BH = BH;
+  p.N = N;
+  p.nc = (N + 127) / 128;
+  p.scale = scale;
+  p.sqrt_scale = std::sqrt(scale);
+  // one CTA per slice, its chunks in order
+  const int grid = BH < ds->num_sms ? BH : ds->num_sms;
+  tk_based_linear_kernel<<<grid, BasedLinCfg::kThreads, BasedLinCfg::kSmemAlloc,
+                           reinterpret_cast<cudaStream_t>(stream)>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? TK_ATTN_OK : TK_ATTN_ERR_LAUNCH;
 }
 

@@ -187,6 +187,18 @@ class BasedWorkload:
         pairs = self.N * self.N / (2 if self.causal else 1)
         return self.B * self.H * pairs * 2.0 * (self.Df + self.Dv)
 
+    @property
+    def linear_flops(self) -> float:
+        """Tensor FLOPs the linear-time kernel (tk_based_fwd_linear) executes:
+        per 128-position chunk Q K^T (K 16) and A V_ext (N 128: the 64 values,
+        the ones column of z, padding); phi(Q) S (K 160) for every chunk but
+        a slice's first, and the state update (N 160) for every chunk but its
+        last."""
+        nc = (self.N + 127) // 128
+        per_chunk = 2.0 * 128 * 128 * (16 + 128)
+        state = 2.0 * 128 * 128 * 160
+        return self.B * self.H * (nc * per_chunk + 2 * (nc - 1) * state)
+
 
 BASED_WORKLOADS = (BasedWorkload("based_n4096_c", 16, 16, 4096, True, 8),)
 BASED_BY_NAME = {w.name: w for w in BASED_WORKLOADS}

@@ -6,7 +6,8 @@
 `--workload bwd_n4096_d128` (or bwd_<any forward workload>) times the backward
 pass, tk_attn_bwd, with the forward's outputs computed beforehand.
 
-`--workload based_n4096_c` times Based linear attention, tk_based_fwd.
+`--workload based_n4096_c` times Based linear attention, tk_based_fwd (the direct
+evaluation) and, beside it, tk_based_fwd_linear (the linear-time kernel).
 
 `--workload gemm_8192` times the library's bf16 GEMM (tk_gemm_bf16, C = A B^T,
 M = N = K = 8192) instead, with cuBLAS (torch.matmul) on the same operands
@@ -391,8 +392,9 @@ def time_bwd(w, steps: int, warmup: int, device):
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
-def time_based(w, steps: int, warmup: int, device):
-    """CUDA-event times of `steps` tk_based_fwd launches, L2 flushed before each."""
+def time_based(w, steps: int, warmup: int, device, linear: bool = False):
+    """CUDA-event times of `steps` tk_based_fwd launches (tk_based_fwd_linear
+    with `linear`, causal workloads only), L2 flushed before each."""
     import torch
 
     from attention_forward_tk_gb300 import api
@@ -405,10 +407,17 @@ def time_based(w, steps: int, warmup: int, device):
     stream = torch.cuda.current_stream(device)
     sh = stream.cuda_stream
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), y.data_ptr(), z.data_ptr(), w.B, w.H, w.N,
-            w.Df, w.Dv, w.scale, int(w.causal), sh)
+            w.Df, w.Dv, w.scale)
+    if linear:
+        assert w.causal
+        call = api.tk_based_fwd_linear
+        args = args + (sh,)
+    else:
+        call = api.tk_based_fwd
+        args = args + (int(w.causal), sh)
     for _ in range(warmup):
         flush.zero_()
-        st = api.tk_based_fwd(*args)
+        st = call(*args)
         if st:
             raise RuntimeError(api.tk_attn_status_string(st))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -417,11 +426,11 @@ def time_based(w, steps: int, warmup: int, device):
     for e0, e1 in evs:
         flush.zero_()
         e0.record(stream)
-        api.tk_based_fwd(*args)
+        call(*args)
         e1.record(stream)
     torch.cuda.synchronize(device)
     if api.tk_attn_last_device_error(sh) != 0:
-        raise RuntimeError("device-side barrier timeout in tk_based_fwd")
+        raise RuntimeError("device-side barrier timeout in the Based kernel")
     return [e0.elapsed_time(e1) for e0, e1 in evs]
 
 
@@ -618,6 +627,15 @@ def main():
             c = oclk.summary()
             extra[bw.name] = {"ms": round(m, 4), "tflops": round(bw.flops / m / 1e9, 1),
                               "launches": 50, "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
+            if bw.causal:
+                with ClockSampler(device.index if world == 1 else local) as oclk:
+                    lms = time_based(bw, 50, 3, device, linear=True)
+                ml = statistics.median(lms)
+                c = oclk.summary()
+                extra[bw.name + "_linear"] = {
+                    "ms": round(ml, 4), "tflops_executed": round(bw.linear_flops / ml / 1e9, 1),
+                    "speedup_vs_direct": round(m / ml, 2), "launches": 50,
+                    "sm_mhz": c["sm_mhz"], "reasons": c["reasons"]}
         for gw in GEMM_WORKLOADS:
             with ClockSampler(device.index if world == 1 else local) as oclk:
                 gms, cms = time_gemm(gw, 100, 5, device)
@@ -737,6 +755,7 @@ def main_based(args, w, world, rank, local):
     build_library()
     with ClockSampler(device.index) as clk:
         ms = time_based(w, args.steps, args.warmup, device)
+        lms = time_based(w, args.steps, args.warmup, device, linear=True) if w.causal else None
     if rank != 0:
         return
     peak_tf, _, peak_kind = measured_peaks()
@@ -757,6 +776,12 @@ def main_based(args, w, world, rank, local):
         "kernel_ms_median": round(statistics.median(ms), 5),
         "clocks": clk.summary(),
     }
+    if lms is not None:
+        tl = statistics.mean(lms)
+        line["linear"] = {"kernel": "tk_based_fwd_linear", "ms_per_step": round(tl, 5),
+                          "tflops_executed": round(w.linear_flops / (tl / 1e3) / 1e12, 1),
+                          "flops_per_step": w.linear_flops, "speedup_vs_direct": round(t / tl, 2)}
+        line["gpu_launches"] = 2 * args.steps
     print(json.dumps(line), flush=True)
 
 

@@ -3,8 +3,9 @@
  *
  * Entry points: tk_attn_fwd (the forward pass, below), tk_attn_fwd_splitkv,
  * tk_attn_fwd_qk and tk_attn_fwd_splitkv_static (queries against a longer
- * key set, keys split into ranges; tk_attn_fwd_qk also causal), tk_attn_bwd (dQ, dK, dV), tk_based_fwd (Based linear
- * attention) and tk_gemm_bf16 (C = A B^T), each with argument checks that
+ * key set, keys split into ranges; tk_attn_fwd_qk also causal), tk_attn_bwd
+ * (dQ, dK, dV), tk_based_fwd and tk_based_fwd_linear (Based linear attention,
+ * direct and linear-time) and tk_gemm_bf16 (C = A B^T), each with argument checks that
  * need no GPU, plus status, version and device-error queries.
  *
  * The operation (one call = one whole forward pass over B*H independent
@@ -72,7 +73,7 @@ typedef struct CUstream_st *tk_attn_stream_t;
 #define TK_ATTN_ERR_TOO_LARGE (-6)      /* tk_attn_fwd_splitkv_static: the ranges'
                                            partial results exceed its static scratch */
 
-#define TK_ATTN_VERSION 10400 /* major*10000 + minor*100 + patch */
+#define TK_ATTN_VERSION 10500 /* major*10000 + minor*100 + patch */
 
 /*
  * tk_attn_fwd -- fused attention forward, asynchronous on `stream`.
@@ -261,6 +262,23 @@ int tk_attn_bwd_check_args(const void *q, const void *k, const void *v, const vo
  */
 int tk_based_fwd(const void *q, const void *k, const void *v, void *y, float *z, int B, int H,
                  int N, int Df, int Dv, float scale, int causal, tk_attn_stream_t stream);
+
+/*
+ * tk_based_fwd_linear -- the causal output of tk_based_fwd through the
+ * linear-time algorithm the pages' Based figure refers to: chunks of 128
+ * positions, the part of each sum inside a chunk evaluated as T(s_ij)
+ * directly, the part before it as phi(q_i) S with the running state
+ * S = sum_j phi(k_j) v_j^T (153 features: the distinct terms of phi) and its
+ * row of sum_j phi(k_j) for z.  Work is linear in N: about 15 MFLOP of
+ * tensor products per 128 positions of a slice, whatever N (the direct
+ * evaluation takes 2 (16 + 64) FLOPs per visible pair).
+ * Products take bf16 operands (phi and a bf16 copy of the fp32 state) with
+ * fp32 accumulation.  Arguments, layouts and errors as tk_based_fwd (always
+ * causal); scale must be >= 0 (the feature maps take sqrt(scale)), else
+ * TK_ATTN_ERR_INVALID_ARG.
+ */
+int tk_based_fwd_linear(const void *q, const void *k, const void *v, void *y, float *z, int B,
+                        int H, int N, int Df, int Dv, float scale, tk_attn_stream_t stream);
 
 /* The argument checks of tk_based_fwd alone (no GPU needed). */
 int tk_based_check_args(const void *q, const void *k, const void *v, const void *y,

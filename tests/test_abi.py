@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol(tk_lib):
 
 
 def test_version_and_status_strings(tk_lib):
-    assert tk_lib.tk_attn_version() == 10400
+    assert tk_lib.tk_attn_version() == 10500
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = tk_lib.tk_attn_status_string(code)
         assert s and s != "unknown status"

@@ -624,6 +624,88 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=(), h
     return roles
 
 
+def based_linear_roles(sim, units):
+    """tk_based_linear_kernel (one CTA): units = chunk counts of its slices.
+    Per chunk the MMA thread issues S_qk, then A V_ext once the warps wrote
+    A and the previous chunk's y was read, then phi(Q) S_ext once the feature
+    panels and (past a slice's first chunk) the state copy are in, then
+    (before a slice's last chunk) the state update.  Buffers are versioned:
+    the feature panels, the state copy in shared memory and the state in
+    tensor memory."""
+    for b in ("s_full", "p_full", "y_full", "y_free", "phi_full", "phi_empty", "st_full",
+              "sx_full"):
+        sim.bar(b)
+    for st in range(2):
+        sim.bar(f"in_full{st}"), sim.bar(f"in_empty{st}")
+
+    def producer():
+        it = 0
+        for nc in units:
+            for _ in range(nc):
+                if it >= 2:
+                    yield ("wait", f"in_empty{it & 1}", (it >> 1) - 1)
+                yield ("commit", f"in_full{it & 1}", "tma")
+                it += 1
+
+    def mma():
+        it = cv = upd = 0
+        for nc in units:
+            for c in range(nc):
+                yield ("wait", f"in_full{it & 1}", it >> 1)
+                yield ("commit", "s_full", None, it)
+                if it > 0:
+                    yield ("wait", "y_free", it - 1)
+                yield ("wait", "p_full", it)
+                yield ("wait", "phi_full", it)
+                yield ("read", "phi", it)             # by phi(Q) S_ext and the update
+                if c > 0:
+                    yield ("wait", "sx_full", cv)
+                    yield ("read", "sext", cv)
+                    cv += 1
+                yield ("commit", "y_full", None, it)
+                if c + 1 < nc:
+                    yield ("write", "state", upd)     # S^T (+)= V_ext^T phi(K)
+                    yield ("commit", "st_full", None, upd)
+                    upd += 1
+                yield ("commit", "phi_empty", None, it)
+                yield ("commit", f"in_empty{it & 1}", None, it >> 1)
+                it += 1
+
+    def twarps():
+        it = 0
+        for nc in units:
+            for _ in range(nc):
+                yield ("wait", "s_full", it)
+                yield ("arrive", "p_full", it)
+                yield ("wait", "y_full", it)
+                yield ("arrive", "y_free", it)
+                it += 1
+
+    def features():
+        it = 0
+        for nc in units:
+            for _ in range(nc):
+                if it > 0:
+                    yield ("wait", "phi_empty", it - 1)
+                yield ("write", "phi", it)
+                yield ("arrive", "phi_full", it)
+                it += 1
+
+    def converter():
+        it = cv = 0
+        for nc in units:
+            for c in range(nc):
+                if c + 1 < nc:
+                    yield ("wait", "st_full", cv)
+                    yield ("read", "state", cv)
+                    yield ("write", "sext", cv)
+                    yield ("arrive", "sx_full", cv)
+                    cv += 1
+                it += 1
+
+    return {"producer": producer(), "mma": mma(), "twarps": twarps(), "features": features(),
+            "converter": converter()}
+
 FWD_UNITS = [
     [(1, 1)], [(1, 2)], [(2, 2)], [(4, 4)],
     [(1, 2), (1, 2), (1, 2)],              # single-step causal units, back to back
@@ -701,9 +783,10 @@ UNIT_LISTS = [[1], [2], [3], [4], [1, 1, 1], [5, 1, 2, 7], [3, 3], [1, 4, 1, 9, 
 
 
 @pytest.mark.parametrize("units", UNIT_LISTS, ids=lambda u: "-".join(map(str, u)))
-@pytest.mark.parametrize("kernel", ["based", "dq", "dkdv"])
+@pytest.mark.parametrize("kernel", ["based", "based_linear", "dq", "dkdv"])
 def test_protocol_completes_without_run_ahead(kernel, units):
-    build = {"based": based_roles, "dq": dq_roles, "dkdv": dkdv_roles}[kernel]
+    build = {"based": based_roles, "based_linear": based_linear_roles, "dq": dq_roles,
+             "dkdv": dkdv_roles}[kernel]
     for seed in range(60):
         sim = Sim(seed)
         sim.run(build(sim, units))
