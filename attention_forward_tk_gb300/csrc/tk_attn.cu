@@ -124,6 +124,12 @@ void init_device(int dev, DeviceState &ds) {
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    BasedLinCfg::kSmemAlloc) != cudaSuccess))
     st = TK_ATTN_ERR_LAUNCH;
+  if (!st) {
+    // its register split (setmaxnreg) assumes 72 registers a thread at launch
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, tk_based_linear_kernel) != cudaSuccess || fa.numRegs != 72)
+      st = TK_ATTN_ERR_LAUNCH;
+  }
   if (!st) st = configure_bwd<64, false>();
   if (!st) st = configure_bwd<64, true>();
   if (!st) st = configure_bwd<128, false>();

@@ -626,14 +626,17 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=(), h
 
 def based_linear_roles(sim, units):
     """tk_based_linear_kernel (one CTA): units = chunk counts of its slices.
-    Per chunk the MMA thread issues S_qk, then A V_ext once the warps wrote
-    A and the previous chunk's y was read, then phi(Q) S_ext once the feature
-    panels and (past a slice's first chunk) the state copy are in, then
-    (before a slice's last chunk) the state update.  Buffers are versioned:
-    the feature panels, the state copy in shared memory and the state in
+    Per chunk the MMA thread issues S_qk; the state update (before a slice's
+    last chunk, once phi(K) is written and the copy warps hold the previous
+    state); A V_ext once A is written and the previous y read; phi(Q) S_ext
+    (past a slice's first chunk) once phi(Q) and the state copy are in.  The
+    copy warps load the updated state, release it, and store the copy once
+    the phi(Q) S_ext products issued before are done.  Versioned buffers:
+    the two feature panels, the state copy in shared memory and the state in
     tensor memory."""
-    for b in ("s_full", "p_full", "y_full", "y_free", "phi_full", "phi_empty", "st_full",
-              "sx_full"):
+    for b in ("s_full", "p_full", "y_full0", "y_full1", "y_free0", "y_free1", "phik_full",
+              "phik_empty", "phiq_full", "phiq_empty", "st_full", "st_read", "sx_full",
+              "sext_free"):
         sim.bar(b)
     for st in range(2):
         sim.bar(f"in_full{st}"), sim.bar(f"in_empty{st}")
@@ -648,63 +651,83 @@ def based_linear_roles(sim, units):
                 it += 1
 
     def mma():
-        it = cv = upd = 0
+        it = cv = ups = upw = dn = 0
         for nc in units:
             for c in range(nc):
                 yield ("wait", f"in_full{it & 1}", it >> 1)
                 yield ("commit", "s_full", None, it)
-                if it > 0:
-                    yield ("wait", "y_free", it - 1)
+                yield ("wait", "phik_full", it)
+                if c + 1 < nc:
+                    if ups > upw:
+                        yield ("wait", "st_read", upw)
+                        upw += 1
+                    yield ("read", "phik", it)
+                    yield ("write", "state", ups)      # S^T (+)= V_ext^T phi(K)
+                    yield ("commit", "st_full", None, ups)
+                    ups += 1
+                yield ("commit", "phik_empty", None, it)
+                if it >= 2:  # the y of the chunk two back, the Y buffer's previous use
+                    yield ("wait", f"y_free{it & 1}", (it >> 1) - 1)
                 yield ("wait", "p_full", it)
-                yield ("wait", "phi_full", it)
-                yield ("read", "phi", it)             # by phi(Q) S_ext and the update
+                yield ("write", f"ybuf{it & 1}", it >> 1)
+                yield ("wait", "phiq_full", it)
                 if c > 0:
                     yield ("wait", "sx_full", cv)
+                    yield ("read", "phiq", it)
                     yield ("read", "sext", cv)
                     cv += 1
-                yield ("commit", "y_full", None, it)
-                if c + 1 < nc:
-                    yield ("write", "state", upd)     # S^T (+)= V_ext^T phi(K)
-                    yield ("commit", "st_full", None, upd)
-                    upd += 1
-                yield ("commit", "phi_empty", None, it)
+                    yield ("commit", "sext_free", None, dn)
+                    dn += 1
+                yield ("commit", f"y_full{it & 1}", None, it >> 1)
+                yield ("commit", "phiq_empty", None, it)
                 yield ("commit", f"in_empty{it & 1}", None, it >> 1)
                 it += 1
 
-    def twarps():
+    def twarps():  # A of a chunk, then the y of the chunk before it
+        def epilogue(e):
+            yield ("wait", f"y_full{e & 1}", e >> 1)
+            yield ("read", f"ybuf{e & 1}", e >> 1)
+            yield ("arrive", f"y_free{e & 1}", e >> 1)
         it = 0
         for nc in units:
             for _ in range(nc):
                 yield ("wait", "s_full", it)
                 yield ("arrive", "p_full", it)
-                yield ("wait", "y_full", it)
-                yield ("arrive", "y_free", it)
+                if it > 0:
+                    yield from epilogue(it - 1)
                 it += 1
+        if it > 0:
+            yield from epilogue(it - 1)
 
-    def features():
+    def features(kind):  # phi(K) and phi(Q) are built by warps of their own
         it = 0
         for nc in units:
-            for _ in range(nc):
+            for c in range(nc):
                 if it > 0:
-                    yield ("wait", "phi_empty", it - 1)
-                yield ("write", "phi", it)
-                yield ("arrive", "phi_full", it)
+                    yield ("wait", f"phi{kind}_empty", it - 1)
+                if (c + 1 < nc) if kind == "k" else (c > 0):
+                    yield ("write", f"phi{kind}", it)
+                yield ("arrive", f"phi{kind}_full", it)
                 it += 1
 
     def converter():
-        it = cv = 0
+        cv = dseen = 0
         for nc in units:
-            for c in range(nc):
-                if c + 1 < nc:
-                    yield ("wait", "st_full", cv)
-                    yield ("read", "state", cv)
-                    yield ("write", "sext", cv)
-                    yield ("arrive", "sx_full", cv)
-                    cv += 1
-                it += 1
+            for c in range(nc - 1):
+                yield ("wait", "st_full", cv)
+                yield ("read", "state", cv)
+                yield ("arrive", "st_read", cv)
+                d = dseen + c
+                if d > 0:
+                    yield ("wait", "sext_free", d - 1)
+                yield ("write", "sext", cv)
+                yield ("arrive", "sx_full", cv)
+                cv += 1
+            dseen += nc - 1
 
-    return {"producer": producer(), "mma": mma(), "twarps": twarps(), "features": features(),
-            "converter": converter()}
+    return {"producer": producer(), "mma": mma(), "twarps": twarps(),
+            "features_k": features("k"), "features_q": features("q"), "converter": converter()}
+
 
 FWD_UNITS = [
     [(1, 1)], [(1, 2)], [(2, 2)], [(4, 4)],
