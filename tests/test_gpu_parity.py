@@ -163,3 +163,6 @@ def test_host_buffer_pieces_match_one_piece(tk_lib):
     o1, l1 = o1.clone(), l1.clone()
     o4, l4 = attention_forward_host(q, k, v, causal=True, chunks=4)
     assert torch.equal(o1, o4) and torch.equal(l1, l4)
+    o1, l1 = o1.clone(), l1.clone()
+    o7, l7 = attention_forward_host(q, k, v, causal=True, chunks=7)  # pieces cut inside batch entries
+    assert torch.equal(o1, o7) and torch.equal(l1, l7)
