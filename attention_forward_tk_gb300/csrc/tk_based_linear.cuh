@@ -355,6 +355,9 @@ __global__ void __launch_bounds__(896, 1)
     const int fh = (warp - 16) >> 2;       // feature half: features 80 fh .. 80 fh + 79
     const int d = (warp & 3) * 32 + lane;  // value column of S = TMEM lane = S_ext row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    // phi(Q) S_ext reads S_ext rows 0 .. 79 (N = 80): the lane quadrant of
+    // rows 96 .. 127 keeps the barriers only, and rows 80 .. 95 are not stored
+    const bool used = (warp & 3) * 32 < (int)C::kYCols;
     uint32_t cv = 0, dseen = 0;  // copies made; phi(Q) S_ext products of earlier slices
     bool ok = true;
     for (int bh = blockIdx.x; bh < p.BH && ok; bh += gridDim.x) {
@@ -366,20 +369,22 @@ __global__ void __launch_bounds__(896, 1)
         }
         tc_fence_after_sync();
         uint4 w[10];  // this warp's 80 features of the row in bf16, 16-byte units
+        if (used) {
 #pragma unroll
-        for (int f0 = 0; f0 < 80; f0 += 16) {
-          uint32_t sv[16];
-          tmem_ld_32x32b_x16(tmem + lane_off + C::kColSt + 80 * fh + f0, sv);
-          tmem_wait_ld();
+          for (int f0 = 0; f0 < 80; f0 += 16) {
+            uint32_t sv[16];
+            tmem_ld_32x32b_x16(tmem + lane_off + C::kColSt + 80 * fh + f0, sv);
+            tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            reg_barrier(sv[8 * u]);
-            reg_barrier(sv[8 * u + 7]);
-            w[(f0 >> 3) + u] = make_uint4(
-                pack_bf16x2(__uint_as_float(sv[8 * u]), __uint_as_float(sv[8 * u + 1])),
-                pack_bf16x2(__uint_as_float(sv[8 * u + 2]), __uint_as_float(sv[8 * u + 3])),
-                pack_bf16x2(__uint_as_float(sv[8 * u + 4]), __uint_as_float(sv[8 * u + 5])),
-                pack_bf16x2(__uint_as_float(sv[8 * u + 6]), __uint_as_float(sv[8 * u + 7])));
+            for (int u = 0; u < 2; ++u) {
+              reg_barrier(sv[8 * u]);
+              reg_barrier(sv[8 * u + 7]);
+              w[(f0 >> 3) + u] = make_uint4(
+                  pack_bf16x2(__uint_as_float(sv[8 * u]), __uint_as_float(sv[8 * u + 1])),
+                  pack_bf16x2(__uint_as_float(sv[8 * u + 2]), __uint_as_float(sv[8 * u + 3])),
+                  pack_bf16x2(__uint_as_float(sv[8 * u + 4]), __uint_as_float(sv[8 * u + 5])),
+                  pack_bf16x2(__uint_as_float(sv[8 * u + 6]), __uint_as_float(sv[8 * u + 7])));
+            }
           }
         }
         // S^T is in registers: the next update may accumulate into it
@@ -394,11 +399,13 @@ __global__ void __launch_bounds__(896, 1)
           ok = false;
           break;
         }
+        if (d < (int)C::kYCols) {
 #pragma unroll
-        for (int u = 0; u < 10; ++u) {
-          const int U = 10 * fh + u;
-          *reinterpret_cast<uint4 *>(sext + (U >> 3) * C::kChunkB + d * 128 +
-                                     (((U & 7) ^ (d & 7)) << 4)) = w[u];
+          for (int u = 0; u < 10; ++u) {
+            const int U = 10 * fh + u;
+            *reinterpret_cast<uint4 *>(sext + (U >> 3) * C::kChunkB + d * 128 +
+                                       (((U & 7) ^ (d & 7)) << 4)) = w[u];
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
