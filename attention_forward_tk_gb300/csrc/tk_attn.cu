@@ -413,12 +413,13 @@ namespace {
 
 // Ranges for a split over keys: `requested` (> 0), or by default the count
 // that minimises the launch's makespan in K/V steps, rounds x (T + c), when
-// that beats one range by at least 10%: units
+// that beats one range by at least 10% (5% with at most 128 queries): units
 // = (slice, query block) pairs x ranges run in ceil(units / SMs) rounds of
 // one unit per SM, and a unit of T tiles costs about c = 3 tiles more for
 // its start and end.  At most one range per 128-key tile, and no empty
 // range: ranges of T tiles, S = ceil(nkv / T).
-void resolve_splits(int requested, long long units_q, int nkv, int num_sms, int *S, int *T) {
+void resolve_splits(int requested, long long units_q, int nkv, int num_sms, int Nq, int *S,
+                    int *T) {
   auto fit = [nkv](long long s, int *S_, int *T_) {
     if (s > nkv) s = nkv;
     if (s < 1) s = 1;
@@ -445,8 +446,12 @@ void resolve_splits(int requested, long long units_q, int nkv, int num_sms, int 
     }
   }
   // The ranges' fp32 partial results make a round trip through memory and a
-  // second kernel: split only for a clearly shorter makespan (>= 10%).
-  if (best < 0 || 10 * best > 9 * one) fit(1, S, T);
+  // second kernel: split only for a clearly shorter makespan, >= 10%, or
+  // >= 5% with at most 128 queries a slice, whose partial results are small
+  // (a decode step: 4 ranges instead of 1 took B8 H32 Nq1 Nk16384 from 0.420
+  // to 0.400 ms on GB300).
+  const long long pct = Nq <= 128 ? 5 : 10;
+  if (best < 0 || 100 * best > (100 - pct) * one) fit(1, S, T);
 }
 
 size_t split_workspace(long long BH, int Nq, int D, int S) {
@@ -490,7 +495,8 @@ extern "C" size_t tk_attn_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, 
   if (!ds) return 0;
   const long long BH = (long long)B * H;
   int S, T;
-  resolve_splits(num_splits, BH * ((Nq + 255LL) / 256), (Nk + 127) / 128, ds->num_sms, &S, &T);
+  resolve_splits(num_splits, BH * ((Nq + 255LL) / 256), (Nk + 127) / 128, ds->num_sms, Nq, &S,
+                 &T);
   return split_workspace(BH, Nq, D, S);
 }
 
@@ -509,7 +515,7 @@ int fwd_qk(const void *q, const void *k, const void *v, void *o, float *lse, int
   const int BH = B * H;
   const int nmb = (Nq + 255) / 256, nkv = (Nk + 127) / 128;
   int S, T;
-  resolve_splits(num_splits, (long long)BH * nmb, nkv, ds->num_sms, &S, &T);
+  resolve_splits(num_splits, (long long)BH * nmb, nkv, ds->num_sms, Nq, &S, &T);
   const size_t need = split_workspace(BH, Nq, D, S);
   FwdParams p;
   p.o = static_cast<__nv_bfloat16 *>(o);
@@ -619,7 +625,8 @@ extern "C" int tk_attn_fwd_splitkv_static(const void *q, const void *k, const vo
   if (!ds) return st;
   const long long BH = (long long)B * H;
   int S, T;
-  resolve_splits(num_splits, BH * ((Nq + 255LL) / 256), (Nk + 127) / 128, ds->num_sms, &S, &T);
+  resolve_splits(num_splits, BH * ((Nq + 255LL) / 256), (Nk + 127) / 128, ds->num_sms, Nq, &S,
+                 &T);
   if (split_workspace(BH, Nq, D, S) > kStaticScratchBytes) return TK_ATTN_ERR_TOO_LARGE;
   return tk_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, D, scale, num_splits,
                              ds->static_scratch, kStaticScratchBytes, stream);
