@@ -60,7 +60,7 @@ struct BwdCfg {
   static constexpr int kKStages = D == 128 ? 3 : 4, kVStages = D == 128 ? 2 : 4;
   static constexpr int kDqSmemAlloc = (2 + kKStages + kVStages) * kTileBytes + 1024;
   static constexpr int kDqThreads = 576;   // dq: 16 elementwise warps, producer, MMA
-  static constexpr int kThreads = 320;            // 8 elementwise warps, producer, MMA
+  static constexpr int kThreads = 576;            // dkdv: 16 elementwise warps, producer, MMA
   // TMEM columns: S (or S^T), dP (or dP^T), and the D-wide accumulators
   static constexpr uint32_t kColS = 0, kColdP = 128, kColA = 256, kColB = 256 + D;
 };
@@ -211,7 +211,7 @@ __device__ __forceinline__ void dq_unit(const BwdParams &p, int u, int &bh, int 
 // S^T_{i+1} overwrites P^T_i and dP^T_{i+1} overwrites dS^T_i only after the
 // MMAs that read them, because one thread issues all MMAs in order.
 template <int D, bool kCausal>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(576, 1)
     tk_attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
@@ -232,16 +232,16 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&sb.ring_empty[s], 1);
     }
     mbar_init(&sb.s_full, 1);
-    mbar_init(&sb.p_full, 8);
+    mbar_init(&sb.p_full, 16);
     mbar_init(&sb.dp_full, 1);
-    mbar_init(&sb.ds_full, 8);
+    mbar_init(&sb.ds_full, 16);
     mbar_init(&sb.acc_full, 1);
-    mbar_init(&sb.acc_empty, 8);
+    mbar_init(&sb.acc_empty, 16);
     mbar_init(&sb.mma_done, 1);
     sb.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 17) {
     tmem_alloc(&sb.tmem_base, 512);
     tmem_relinquish();
   }
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(320, 1)
     atomicCAS(p.err, 0, kDevErrTimeout);
   };
 
-  if (warp < 8) {
+  if (warp < 16) {
     // ---------------------------------------------------------- elementwise
     const int qd = warp & 3, h = warp >> 2;
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
@@ -278,11 +278,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         tc_fence_after_sync();
         const bool edge = (kCausal && i == j) || (i * 128 + 128 > p.N);
-        // P^T = exp2(S^T scale log2(e) - LSE_i log2(e)), masked -> 0; kept in fp32
-        uint64_t pr[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * h + 32 * c;
+        // P^T = exp2(S^T scale log2(e) - LSE_i log2(e)), masked -> 0; kept in fp32.
+        // Warp (qd, h) takes query columns 32 h .. 32 h + 31 of its lane quadrant.
+        uint64_t pr[16];
+        {
+          const int c = 0;
+          const int col0 = 32 * h;
           uint32_t sv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + C::kColS + col0, sv);
           tmem_wait_ld();
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(320, 1)
             pr[16 * c + (t >> 1)] = f2_pack(p0, p1);
             pk[t >> 1] = pack_bf16x2(p0, p1);
           }
-          tmem_st_32x32b_x16(tmem + lane_off + C::kColS + 64 * h + 16 * c, pk);
+          tmem_st_32x32b_x16(tmem + lane_off + C::kColS + 32 * h, pk);
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -318,9 +319,9 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after_sync();
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * h + 32 * c;
+        {
+          const int c = 0;
+          const int col0 = 32 * h;
           uint32_t dv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + C::kColdP + col0, dv);
           tmem_wait_ld();
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(320, 1)
                       d0, d1);
             dk[t >> 1] = pack_bf16x2(d0, d1);
           }
-          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 64 * h + 16 * c, dk);
+          tmem_st_32x32b_x16(tmem + lane_off + C::kColdP + 32 * h, dk);
         }
         tmem_wait_st();
         tc_fence_before_sync();
@@ -353,13 +354,14 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after_sync();
       const bool valid = kj < p.N;
       const size_t row_off = ((size_t)bh * p.N + (valid ? kj : 0)) * D;
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
+      {
+        // warps h = 0, 1 write dV, h = 2, 3 write scale * dK, each half the columns
+        const int g = h >> 1;
         const uint32_t col = g ? C::kColB : C::kColA;
         __nv_bfloat16 *dst = (g ? p.dk : p.dv) + row_off;
         const float mul = g ? p.scale : 1.f;
 #pragma unroll 1
-        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+        for (int c0 = (h & 1) * (D / 2); c0 < ((h & 1) + 1) * (D / 2); c0 += 32) {
           uint32_t rv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + col + c0, rv);
           tmem_wait_ld();
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sb.acc_empty);
     }
-  } else if (warp == 8 && lane == 0) {
+  } else if (warp == 16 && lane == 0) {
     // ---------------------------------------------------------- TMA producer
     uint32_t it = 0, uc = 0;
     bool ok = true;
@@ -423,7 +425,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     // copies still in flight land before the CTA can exit
     for (int i = 0; i < 200 && !ok; ++i) __nanosleep(1000);
-  } else if (warp == 9 && lane == 0) {
+  } else if (warp == 17 && lane == 0) {
     // ---------------------------------------------------------- MMA issue
     constexpr uint32_t idS = idesc_f32acc(true, 128, 128, false, false);
     constexpr uint32_t idG = idesc_f32acc(true, 128, D, false, true);
@@ -466,7 +468,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         tc_fence_after_sync();
         // dV += P^T dO (B operand MN-major), then the next step's S^T
-        issue_grad(tmem + C::kColA, tmem + C::kColS, sdesc_sw128_lo(sdo, C::kChunkBytes), dhi,
+        issue_grad<4>(tmem + C::kColA, tmem + C::kColS, sdesc_sw128_lo(sdo, C::kChunkBytes), dhi,
                    idG, acc);
         const bool more = st + 1 < n;
         if (more) {
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         tc_fence_after_sync();
         // dK += dS^T Q, then the next step's dP^T
-        issue_grad(tmem + C::kColB, tmem + C::kColdP, sdesc_sw128_lo(sq, C::kChunkBytes), dhi,
+        issue_grad<4>(tmem + C::kColB, tmem + C::kColdP, sdesc_sw128_lo(sq, C::kChunkBytes), dhi,
                    idG, acc);
         umma_commit(&sb.ring_empty[it % C::kStages]);
         if (more) {
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(320, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 17) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
