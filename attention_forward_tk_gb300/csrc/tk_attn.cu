@@ -51,6 +51,10 @@ struct DeviceState {
   int *err_word = nullptr;  // address of g_dev_error on this device
   void *static_scratch = nullptr;  // address of g_splitkv_scratch on this device
   int gemm_pairs = 0;  // CTA pairs of tk_gemm_kernel that fit on the device at once
+  // tk_based_linear_kernel's register split (setmaxnreg) assumes 72
+  // registers a thread at launch; a build that gives it another count
+  // disables that entry point alone
+  bool based_linear_ok = false;
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -125,10 +129,9 @@ void init_device(int dev, DeviceState &ds) {
                                    BasedLinCfg::kSmemAlloc) != cudaSuccess))
     st = TK_ATTN_ERR_LAUNCH;
   if (!st) {
-    // its register split (setmaxnreg) assumes 72 registers a thread at launch
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, tk_based_linear_kernel) != cudaSuccess || fa.numRegs != 72)
-      st = TK_ATTN_ERR_LAUNCH;
+    ds.based_linear_ok =
+        cudaFuncGetAttributes(&fa, tk_based_linear_kernel) == cudaSuccess && fa.numRegs == 72;
   }
   if (!st) st = configure_bwd<64, false>();
   if (!st) st = configure_bwd<64, true>();
@@ -829,6 +832,7 @@ extern "C" int tk_based_fwd_linear(const void *q, const void *k, const void *v, 
   if (!(scale >= 0.f)) return TK_ATTN_ERR_INVALID_ARG;  // the feature maps take sqrt(scale)
   DeviceState *ds = current_device(&st);
   if (!ds) return st;
+  if (!ds->based_linear_ok) return TK_ATTN_ERR_LAUNCH;
   const int BH = B * H;
   CUtensorMap tq, tk, tv;
   if (!make_map_feat(&tq, q, BH, N) || !make_map_feat(&tk, k, BH, N) ||

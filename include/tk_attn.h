@@ -275,7 +275,9 @@ int tk_based_fwd(const void *q, const void *k, const void *v, void *y, float *z,
  * Products take bf16 operands (phi and a bf16 copy of the fp32 state) with
  * fp32 accumulation.  Arguments, layouts and errors as tk_based_fwd (always
  * causal); scale must be >= 0 (the feature maps take sqrt(scale)), else
- * TK_ATTN_ERR_INVALID_ARG.
+ * TK_ATTN_ERR_INVALID_ARG.  TK_ATTN_ERR_LAUNCH also when the kernel was built
+ * with other than the 72 registers a thread its warp roles are split for
+ * (checked once per device; the other entry points are unaffected).
  */
 int tk_based_fwd_linear(const void *q, const void *k, const void *v, void *y, float *z, int B,
                         int H, int N, int Df, int Dv, float scale, tk_attn_stream_t stream);
