@@ -193,7 +193,7 @@ def based_roles(sim, units, S=8, NB=3):
     return {"producer": producer(), "mma": mma(), "warps": warps()}
 
 
-def dq_roles(sim, units, KS=3, VS=2):
+def dq_roles(sim, units, KS=3, VS=2, drop=()):
     """tk_attn_bwd_dq_kernel: two 128-column buffers, step j in buffer j mod
     2 (S_j, then dP_j over it once the warps hold S_j in registers, then bf16
     dS_j over dP_j), separate K and V rings.  Buffer contents are versioned:
@@ -232,7 +232,8 @@ def dq_roles(sim, units, KS=3, VS=2):
             yield ("write", f"buf{it & 1}", 3 * it)        # S_it
             yield ("commit", "s_full", None, it)
             for j in range(n):
-                yield ("wait", "s_read", it)
+                if "s_read" not in drop:
+                    yield ("wait", "s_read", it)
                 yield ("wait", f"v_full{it % VS}", it // VS)
                 yield ("write", f"buf{it & 1}", 3 * it + 1)    # dP_it over S_it
                 yield ("commit", "dp_full", None, it)
@@ -624,7 +625,7 @@ def fwd_roles(sim, units, split_p, S=None, QB=None, single_fin=False, drop=(), h
     return roles
 
 
-def based_linear_roles(sim, units):
+def based_linear_roles(sim, units, drop=()):
     """tk_based_linear_kernel (one CTA): units = chunk counts of its slices.
     Per chunk the MMA thread issues S_qk; the state update (before a slice's
     last chunk, once phi(K) is written and the copy warps hold the previous
@@ -718,7 +719,7 @@ def based_linear_roles(sim, units):
                 yield ("read", "state", cv)
                 yield ("arrive", "st_read", cv)
                 d = dseen + c
-                if d > 0:
+                if d > 0 and "sext_free" not in drop:
                     yield ("wait", "sext_free", d - 1)
                 yield ("write", "sext", cv)
                 yield ("arrive", "sx_full", cv)
@@ -864,5 +865,23 @@ def test_forward_model_sees_a_missing_wait(split_p, drop):
             sim.run(fwd_roles(sim, [(3, 4), (2, 3), (4, 4)], split_p, drop=(drop,)))
         except AssertionError as e:
             assert "uses data" in str(e) or "completed" in str(e), str(e)
+            failures += 1
+    assert failures > 0
+
+
+@pytest.mark.parametrize("kernel,drop", [("dq", "s_read"), ("based_linear", "sext_free")])
+def test_buffer_models_see_a_missing_wait(kernel, drop):
+    """The buffer versions are live: without the dQ warps' "S read" signal
+    the dP product can overwrite S before the warps load it, and without
+    the release of the old state copy the linear Based copy warps can
+    overwrite it while phi(Q) S_ext still reads it."""
+    build = {"dq": dq_roles, "based_linear": based_linear_roles}[kernel]
+    failures = 0
+    for seed in range(300):
+        sim = Sim(seed)
+        try:
+            sim.run(build(sim, [5, 3, 4], drop=(drop,)))
+        except AssertionError as e:
+            assert "version" in str(e) or "completed" in str(e) or "phase" in str(e), str(e)
             failures += 1
     assert failures > 0
