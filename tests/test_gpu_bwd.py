@@ -118,14 +118,18 @@ def test_bwd_rejects_short_workspace(tk_lib):
     assert (t[5] == 3.0).all()
 
 
-@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_bwd_full_size_sampled_slices(tk_lib, oracle_lib, causal):
-    """B16 H16 N4096 D128 (the n4096_d128 shape; causal at B8 H16), the whole
-    launch on the GPU, two (batch, head) slices checked in full."""
-    B, H, N, D = (8 if causal else 16), 16, 4096, 128
+@pytest.mark.parametrize("shape", [(16, 16, 4096, False), (8, 16, 4096, True),
+                                   (8, 16, 8192, True)],
+                         ids=["n4096", "n4096_causal", "n8192_causal"])
+def test_bwd_full_size_sampled_slices(tk_lib, oracle_lib, shape):
+    """The timed backward shapes (B16 H16 N4096 D128, and B8 H16 N8192 D128
+    causal) and a causal N4096 one, the whole launch on the GPU, four (batch,
+    head) slices spread over the launch checked in full."""
+    B, H, N, causal = shape
+    D = 128
     q, k, v = draw((B, H, N, D), 2)
     do = draw_grad((B, H, N, D), 2)
     scale = 1.0 / math.sqrt(D)
     got = run_fwd_bwd(tk_lib, q, k, v, do, scale, causal)
-    slices = [0, B * H - 1]
+    slices = [0, B * H // 3, 2 * B * H // 3 + 1, B * H - 1]
     check(got, oracle_lib.attention_bwd(q, k, v, do, scale, causal, slices=slices), slices)
