@@ -14,10 +14,11 @@ Contents
                    (inference shape); causal aligned to the last key
   attention_bwd    dQ, dK, dV of the same definition for a given dO (numpy,
                    fp64), with the magnitude sums that bound kernel rounding
-  based_quadratic, based_recurrent
+  based_quadratic, based_recurrent, based_rows
                    Based linear attention (Taylor-2 feature map): the
-                   definition evaluated directly, and through explicit feature
-                   maps with a running state (causal)
+                   definition evaluated directly, through explicit feature
+                   maps with a running state (causal), and directly for
+                   chosen causal rows only
   gemm_abt         C = A B^T for bf16 A [M, K], B [N, K] in float64, with the
                    per-element magnitude sum that bounds fp32 accumulation
   tiled_online_softmax
@@ -36,7 +37,7 @@ log over scaled, masked scores).
 from .brute import (attention, attention_qk, attention_qk_rows, attention_rows, build, lib_path,
                     max_threads)
 from .backward import attention_bwd
-from .based import based_quadratic, based_recurrent
+from .based import based_quadratic, based_recurrent, based_rows
 from .gemm import gemm_abt
 from .tiled import tiled_online_softmax
 
@@ -44,6 +45,7 @@ __all__ = [
     "attention_bwd",
     "based_quadratic",
     "based_recurrent",
+    "based_rows",
     "attention",
     "attention_qk",
     "attention_qk_rows",

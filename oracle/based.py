@@ -58,6 +58,31 @@ def based_quadratic(q, k, v, scale: float, causal: bool):
     return y, z, mag
 
 
+def based_rows(q, k, v, scale: float, rows):
+    """Causal y, z and the magnitude sum for chosen rows only, straight from
+    the definition above: row i of slice b*H + h (flat index (b*H + h)*N + i)
+    sums T(scale q_i.k_j) over its keys j <= i.  Memory and time grow with N
+    per row, so long sequences can be checked on a sample.
+    Returns y [R, Dv], z [R], mag [R, Dv]."""
+    Q, K, V = _widen(q), _widen(k), _widen(v)
+    if Q.shape != K.shape or Q.shape[:3] != V.shape[:3] or Q.ndim != 4:
+        raise ValueError("q, k must be [B, H, N, Df] and v [B, H, N, Dv]")
+    B, H, N, Df = Q.shape
+    Dv = V.shape[-1]
+    Qf, Kf, Vf = Q.reshape(B * H, N, Df), K.reshape(B * H, N, Df), V.reshape(B * H, N, Dv)
+    rows = np.asarray(rows, dtype=np.int64)
+    y = np.empty((rows.size, Dv))
+    z = np.empty(rows.size)
+    mag = np.empty((rows.size, Dv))
+    for r, flat in enumerate(rows):
+        bh, i = divmod(int(flat), N)
+        a = taylor2(scale * (Kf[bh, : i + 1] @ Qf[bh, i]))
+        z[r] = a.sum()
+        y[r] = (a @ Vf[bh, : i + 1]) / z[r]
+        mag[r] = (a @ np.abs(Vf[bh, : i + 1])) / z[r]
+    return y, z, mag
+
+
 def feature_map(x, scale: float):
     """phi(sqrt(scale) x) for rows x [..., Df]: [1, x', vec(x' x'^T)/sqrt(2)]."""
     x = np.sqrt(scale) * x

@@ -186,3 +186,31 @@ def test_based_linear_full_size_sampled_slices(tk_lib, oracle_lib):
     yd, zd = run_based(tk_lib, q, k, v, w.scale, True)
     assert np.abs(y - yd).max() <= 2.0 ** -5
     assert (np.abs(z - zd) <= 2.0 ** -6 * zd).all()
+
+
+def _long_rows(BH, N, seed):
+    """Chunk and tile edges, the middle, the last rows and 30 random rows of
+    every slice, as flat indices (b*H + h)*N + i."""
+    rng = np.random.default_rng(seed)
+    per = {0, 1, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1}
+    rows = []
+    for bh in range(BH):
+        idx = sorted(per | set(rng.integers(0, N, 30).tolist()))
+        rows.extend(bh * N + i for i in idx)
+    return np.asarray(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("N", [65536, 65536 + 77])
+def test_based_long_sequence_sampled_rows(tk_lib, oracle_lib, N):
+    """Sequences 16x the timed one (512 chunks through the linear-time
+    kernel's running state; rows of 512 key tiles in the direct kernel), both
+    kernels, causal, on sampled rows against the oracle's per-row evaluation
+    of the definition."""
+    B, H, scale = 1, 4, 0.25
+    q, k, v = draw_based(B, H, N, seed=1500 + N)
+    rows = _long_rows(B * H, N, seed=N)
+    ry, rz, mag = oracle_lib.based_rows(q, k, v, scale, rows)
+    yl, zl = run_based_linear(tk_lib, q, k, v, scale)
+    check_linear(yl.reshape(-1, 64)[rows], zl.reshape(-1)[rows], ry, rz, mag)
+    yd, zd = run_based(tk_lib, q, k, v, scale, True)
+    check(yd.reshape(-1, 64)[rows], zd.reshape(-1)[rows], ry, rz, mag)

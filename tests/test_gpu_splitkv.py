@@ -184,3 +184,25 @@ def test_qk_causal_rejects_more_queries_than_keys(tk_lib):
     st, o, lse = run_qk(tk_lib, q, k, v, 0.125, True, 0)
     assert st == tk_lib.TK_ATTN_ERR_INVALID_ARG
     assert np.isnan(o).all() and np.isnan(lse).all()  # outputs untouched
+
+
+@pytest.mark.parametrize("case", [(1, 8, 1, 262144 + 33, False), (1, 8, 5, 262144 + 33, True)],
+                         ids=["decode_256k", "q5_256k_causal"])
+def test_long_key_range_all_rows(tk_lib, oracle_lib, case):
+    """A quarter million cached keys (16x the timed decode shape): the
+    default split over keys, every query row against the oracle.  Peaky
+    inputs (4 N(0,1) queries and keys, Student-t V), so that O is of order one
+    rather than a near-zero average of 2.6*10^5 rows."""
+    from attention_forward_tk_gb300.inputs import draw
+    B, H, Nq, Nk, causal = case
+    D = 128
+    q, k, v = draw((B, H, Nq, D), 1700 + Nq, "peaky_t3", kv_shape=(B, H, Nk, D))
+    scale = 1 / math.sqrt(D)
+    st, o, lse = run_qk(tk_lib, q, k, v, scale, causal, 0)
+    assert st == 0, tk_lib.tk_attn_status_string(st)
+    o_ref, lse_ref = oracle_lib.attention_qk(q, k, v, scale, causal)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    do = np.abs(o - o_ref)
+    assert do.max() <= TOL_O_MAX, do.max()
+    assert do.mean() <= TOL_O_MEAN, do.mean()
+    assert np.abs(lse - lse_ref).max() <= TOL_LSE_MAX

@@ -532,3 +532,19 @@ def test_based_causal_last_row_sees_everything(oracle_lib):
     np.testing.assert_allclose(yc[:, :, -1], yn[:, :, -1], rtol=1e-13)
     np.testing.assert_allclose(zc[:, :, -1], zn[:, :, -1], rtol=1e-13)
     assert (mc >= np.abs(yc) - 1e-12).all()
+
+
+def test_based_rows_match_the_recurrent_form(oracle_lib):
+    # the per-row evaluation against the running-state form (an independent
+    # route through explicit feature maps), on rows of every slice
+    g = torch.Generator().manual_seed(631)
+    q, k = (torch.randn((2, 2, 40, 4), generator=g).to(torch.bfloat16) for _ in range(2))
+    v = torch.randn((2, 2, 40, 3), generator=g).to(torch.bfloat16)
+    rows = [0, 1, 39, 40, 77, 80 + 17, 159]
+    y, z, mag = oracle_lib.based_rows(q, k, v, 0.4, rows)
+    yr, zr = oracle_lib.based_recurrent(q, k, v, 0.4)
+    np.testing.assert_allclose(z, zr.reshape(-1)[rows], rtol=1e-12)
+    np.testing.assert_allclose(y, yr.reshape(-1, 3)[rows], rtol=1e-10, atol=1e-12)
+    assert (mag >= np.abs(y) - 1e-12).all()
+    # row 0 of a slice sees its own key alone: y = v_0
+    np.testing.assert_array_equal(y[0], widen(v)[0, 0, 0])
