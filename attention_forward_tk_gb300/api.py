@@ -31,6 +31,9 @@ TK_ATTN_ERR_TOO_LARGE = -6
 # every symbol include/tk_attn.h declares
 EXPORTED = (
     "tk_attn_fwd",
+    "tk_attn_fwd_host",
+    "tk_attn_fwd_host_workspace_bytes",
+    "tk_attn_fwd_host_check_args",
     "tk_attn_fwd_splitkv",
     "tk_attn_fwd_qk",
     "tk_attn_fwd_splitkv_static",
@@ -80,6 +83,14 @@ def library() -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.tk_attn_fwd.restype = i
         lib.tk_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.tk_attn_fwd_host.restype = i
+        lib.tk_attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp,
+                                         ctypes.c_size_t, vp]
+        lib.tk_attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.tk_attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i]
+        lib.tk_attn_fwd_host_check_args.restype = i
+        lib.tk_attn_fwd_host_check_args.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp,
+                                                    ctypes.c_size_t]
         lib.tk_attn_fwd_splitkv.restype = i
         lib.tk_attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
                                             ctypes.c_size_t, vp]
@@ -129,6 +140,27 @@ def tk_attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int
                 D: int, scale: float, causal: int, stream: int) -> int:
     return int(library().tk_attn_fwd(q, k, v, o, lse, B, H, N, D, ctypes.c_float(scale),
                                      int(causal), stream))
+
+
+def tk_attn_fwd_host(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int,
+                     D: int, scale: float, causal: int, pieces: int, workspace: int,
+                     workspace_bytes: int, stream: int) -> int:
+    return int(library().tk_attn_fwd_host(q, k, v, o, lse, B, H, N, D, ctypes.c_float(scale),
+                                          int(causal), int(pieces), workspace,
+                                          int(workspace_bytes), stream))
+
+
+def tk_attn_fwd_host_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return int(library().tk_attn_fwd_host_workspace_bytes(B, H, N, D))
+
+
+def tk_attn_fwd_host_check_args(q: int, k: int, v: int, o: int, lse: int, B: int, H: int,
+                                N: int, D: int, scale: float, causal: int, pieces: int,
+                                workspace: int, workspace_bytes: int) -> int:
+    return int(library().tk_attn_fwd_host_check_args(q, k, v, o, lse, B, H, N, D,
+                                                     ctypes.c_float(scale), int(causal),
+                                                     int(pieces), workspace,
+                                                     int(workspace_bytes)))
 
 
 def tk_attn_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Nq: int,
@@ -407,75 +439,40 @@ def gemm_bf16(a, b, out=None, stream=None):
     return out
 
 
-_copy_streams = {}
-
-
-def _side_streams(device):
-    """Two streams per device for the host-buffer call's copies, made once."""
-    import torch
-    key = device.index
-    if key not in _copy_streams:
-        _copy_streams[key] = (torch.cuda.Stream(device), torch.cuda.Stream(device))
-    return _copy_streams[key]
-
-
 def attention_forward_host(q, k, v, causal: bool = False, scale: float | None = None,
-                           device_buffers=None, out=None, lse=None, stream=None,
+                           workspace=None, out=None, lse=None, stream=None,
                            chunks: int | None = None):
-    """The same call for bf16 tensors in (preferably pinned) host memory.
-
-    Copies q, k, v to the device, runs tk_attn_fwd, copies O and LSE back into
-    host tensors `out` / `lse` (allocated pinned when not given) and waits for
-    the work to finish.  `device_buffers` = (q_d, k_d, v_d, o_d, lse_d) reuses
-    device memory between calls.  Returns (out, lse) on the host.
-
-    The B*H (batch, head) slices, independent problems, are cut into
-    `chunks` pieces of whole slices, pipelined over three streams: the
-    host-to-device copies of piece c + 1 and the device-to-host copies of
-    piece c - 1 overlap the kernel on piece c, which runs on `stream`
-    (default: the current stream).  The copies set the pace, so more pieces
-    shorten the unoverlapped kernel and copy-back of the last one; by
-    default up to 32 pieces, each of at least two waves of 256-query units
-    on the device's SMs (B4 H32 N16384 causal: 26 pieces, 9.0 ms a call
-    against 10.7 ms with 4).
-    """
+    """The same call for bf16 tensors in (preferably pinned) host memory,
+    through tk_attn_fwd_host: the library copies q, k, v to the device, runs
+    the forward pass and copies O and LSE back into host tensors `out` /
+    `lse` (allocated pinned when not given), pipelined over `chunks` pieces
+    of whole (batch, head) slices (None: the library's default); then this
+    function waits for the stream.  `workspace` is a device uint8 tensor of at
+    least tk_attn_fwd_host_workspace_bytes(B, H, N, D) bytes, reused between
+    calls when given.  Returns (out, lse) on the host."""
     import torch
     B, H, N, D = (int(x) for x in q.shape)
+    if not (q.shape == k.shape == v.shape) or q.dtype != torch.bfloat16 or q.is_cuda:
+        raise ValueError("q, k, v must be bf16 host tensors of one [B, H, N, D] shape")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
     dev = torch.device("cuda", torch.cuda.current_device())
-    if device_buffers is None:
-        device_buffers = (torch.empty_like(q, device=dev), torch.empty_like(k, device=dev),
-                          torch.empty_like(v, device=dev), torch.empty_like(q, device=dev),
-                          torch.empty((B, H, N), dtype=torch.float32, device=dev))
-    qd, kd, vd, od, ld = device_buffers
+    need = tk_attn_fwd_host_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
-    s = torch.cuda.current_stream() if stream is None else stream
-    s_in, s_out = _side_streams(dev)
-    BH = B * H
-    if chunks is None:
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        chunks = min(32, BH * ((N + 255) // 256) // (2 * sms))
-    pieces = max(1, min(int(chunks), BH))
-    bounds = [BH * c // pieces for c in range(pieces + 1)]
-    # [1, slices, N, D] views of the (batch, head)-flattened tensors
-    flat = [t.reshape(1, BH, *t.shape[2:]) for t in (q, k, v, qd, kd, vd, od, ld, out, lse)]
-    qh, kh, vh, qdf, kdf, vdf, odf, ldf, oh, lh = flat
-    s_in.wait_stream(s)
-    for c in range(pieces):
-        sl = (slice(None), slice(bounds[c], bounds[c + 1]))
-        with torch.cuda.stream(s_in):
-            qdf[sl].copy_(qh[sl], non_blocking=True)
-            kdf[sl].copy_(kh[sl], non_blocking=True)
-            vdf[sl].copy_(vh[sl], non_blocking=True)
-        s.wait_stream(s_in)
-        attention_forward(qdf[sl], kdf[sl], vdf[sl], causal, scale, out=odf[sl], lse=ldf[sl],
-                          stream=s)
-        s_out.wait_stream(s)
-        with torch.cuda.stream(s_out):
-            oh[sl].copy_(odf[sl], non_blocking=True)
-            lh[sl].copy_(ldf[sl], non_blocking=True)
-    s.wait_stream(s_out)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    st = tk_attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, H, N, D, float(scale), int(bool(causal)),
+                          0 if chunks is None else int(chunks), workspace.data_ptr(),
+                          workspace.numel(), _stream_handle(s))
+    if st != TK_ATTN_OK:
+        raise TkAttnError(f"tk_attn_fwd_host: {tk_attn_status_string(st)} ({st})", st)
     s.synchronize()
     return out, lse

@@ -1,6 +1,7 @@
 """Compile the CUDA library in-tree: ``_build/libtk_attn.so`` for sm_103a.
 
-One translation unit (host launcher + kernels), one ``-gencode``; no cmake.
+Two translation units (host launcher + kernels; the host-buffer pipeline),
+one ``-gencode``; no cmake.
 The same command works on x86_64 and aarch64 hosts.
 """
 from __future__ import annotations
@@ -15,7 +16,7 @@ CSRC = os.path.join(_HERE, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 BUILD_DIR = os.path.join(_HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "libtk_attn.so")
-SOURCES = [os.path.join(CSRC, "tk_attn.cu")]
+SOURCES = [os.path.join(CSRC, "tk_attn.cu"), os.path.join(CSRC, "tk_attn_host.cpp")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
     os.path.join(INCLUDE, "tk_attn.h")]
 

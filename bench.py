@@ -449,9 +449,6 @@ def time_e2e(w, steps: int, warmup: int, device):
     from attention_forward_tk_gb300.inputs import workload_inputs
 
     q, k, v = (t.cpu().pin_memory() for t in workload_inputs(w, device=device))
-    bufs = (torch.empty_like(q, device=device), torch.empty_like(k, device=device),
-            torch.empty_like(v, device=device), torch.empty_like(q, device=device),
-            torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device))
     o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, pin_memory=True)
     if w.Nk:
@@ -460,6 +457,10 @@ def time_e2e(w, steps: int, warmup: int, device):
         from attention_forward_tk_gb300.api import tk_attn_splitkv_workspace_bytes
         need = tk_attn_splitkv_workspace_bytes(w.B, w.H, w.N, w.Nk, w.D, 0)
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+
+        bufs = (torch.empty_like(q, device=device), torch.empty_like(k, device=device),
+                torch.empty_like(v, device=device), torch.empty_like(q, device=device),
+                torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device))
 
         def step():
             qd, kd, vd, od, ld = bufs
@@ -471,8 +472,14 @@ def time_e2e(w, steps: int, warmup: int, device):
             lse.copy_(ld, non_blocking=True)
             torch.cuda.current_stream(device).synchronize()
     else:
+        # the C call with host buffers (tk_attn_fwd_host): copies pipelined
+        # with the kernel inside the library
+        from attention_forward_tk_gb300.api import tk_attn_fwd_host_workspace_bytes
+        ws = torch.empty(tk_attn_fwd_host_workspace_bytes(w.B, w.H, w.N, w.D), dtype=torch.uint8,
+                         device=device)
+
         def step():
-            attention_forward_host(q, k, v, w.causal, w.scale, bufs, o, lse)
+            attention_forward_host(q, k, v, w.causal, w.scale, ws, o, lse)
     for _ in range(warmup):
         step()
     stream = torch.cuda.current_stream(device)
@@ -687,7 +694,9 @@ def main():
                       "hbm_peak_gbs": peak_hbm}),
         "e2e": None if args.no_e2e else {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
+                "ms_per_step": round(e2e_ms, 4),
+                "call": "tk_attn_splitkv via torch copies" if w.Nk else
+                        "tk_attn_fwd_host (C ABI, pinned host buffers)"},
         "gpu_launches": launches,
         "wall_s_timed_region": round(wall, 4),
         "kernel_ms_median": round(statistics.median(ms), 5),

@@ -1,7 +1,8 @@
 /*
  * tk_attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
  *
- * Entry points: tk_attn_fwd (the forward pass, below), tk_attn_fwd_splitkv,
+ * Entry points: tk_attn_fwd (the forward pass, below), tk_attn_fwd_host (the
+ * same from and to host memory, copies pipelined with the kernel), tk_attn_fwd_splitkv,
  * tk_attn_fwd_qk and tk_attn_fwd_splitkv_static (queries against a longer
  * key set, keys split into ranges; tk_attn_fwd_qk also causal), tk_attn_bwd
  * (dQ, dK, dV), tk_based_fwd and tk_based_fwd_linear (Based linear attention,
@@ -73,7 +74,7 @@ typedef struct CUstream_st *tk_attn_stream_t;
 #define TK_ATTN_ERR_TOO_LARGE (-6)      /* tk_attn_fwd_splitkv_static: the ranges'
                                            partial results exceed its static scratch */
 
-#define TK_ATTN_VERSION 10500 /* major*10000 + minor*100 + patch */
+#define TK_ATTN_VERSION 10600 /* major*10000 + minor*100 + patch */
 
 /*
  * tk_attn_fwd -- fused attention forward, asynchronous on `stream`.
@@ -106,6 +107,52 @@ int tk_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse
 int tk_attn_check_args(const void *q, const void *k, const void *v, const void *o,
                        const float *lse, int B, int H, int N, int D, float scale,
                        int causal);
+
+/*
+ * tk_attn_fwd_host -- tk_attn_fwd with Q, K, V read from, and O, LSE
+ * written to, HOST memory: the operation is the one above; this call adds
+ * the movement between host and device.  Same shapes, layouts, scale and
+ * mask as tk_attn_fwd; q, k, v, o, lse are host pointers (page-locked
+ * memory, e.g. from cudaHostAlloc, lets the copies overlap the kernel;
+ * pageable memory works, with copies the runtime may stage synchronously).
+ *
+ * The B*H independent (batch, head) slices are cut into `pieces` runs of
+ * whole slices (0 = the default: up to 32 pieces of at least two waves of
+ * 256-query units each on the device's SMs; clamped to [1, min(64, B*H)]).
+ * Piece c's host-to-device copies run on a copy-in stream, its tk_attn_fwd
+ * launch on `stream`, its device-to-host copies on a copy-out stream, so the
+ * copies of neighbouring pieces overlap the kernel.  The library creates
+ * the two side streams and their events once per device; calls on one
+ * device enqueue their work one at a time.
+ *
+ * workspace / workspace_bytes: caller-owned DEVICE memory of at least
+ * tk_attn_fwd_host_workspace_bytes(B, H, N, D) bytes, 256-byte aligned,
+ * holding the device copies of Q, K, V, O and LSE.  It must not be in use
+ * by other work while the call's work runs.
+ *
+ * Ordering: the call's work starts after the work enqueued on `stream`
+ * before it, and `stream` reaches its next work only after the call's last
+ * copy-out: O and LSE are valid on the host once the stream reaches that
+ * point (synchronise the stream before reading them).
+ *
+ * Errors: those of tk_attn_check_args (before any CUDA call, nothing
+ * enqueued, outputs untouched); TK_ATTN_ERR_INVALID_ARG also for pieces < 0
+ * or a missing, misaligned, short or overlapping workspace; _ARCH, _LAUNCH.
+ * A CUDA error after the first piece was enqueued returns _LAUNCH with
+ * that piece's work still enqueued (and ordered before `stream`'s next work).
+ */
+int tk_attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int N, int D, float scale, int causal, int pieces,
+                     void *workspace, size_t workspace_bytes, tk_attn_stream_t stream);
+
+/* Device workspace tk_attn_fwd_host needs (0 for invalid sizes). */
+size_t tk_attn_fwd_host_workspace_bytes(int B, int H, int N, int D);
+
+/* The argument checks of tk_attn_fwd_host alone (no GPU needed). */
+int tk_attn_fwd_host_check_args(const void *q, const void *k, const void *v, const void *o,
+                                const float *lse, int B, int H, int N, int D, float scale,
+                                int causal, int pieces, const void *workspace,
+                                size_t workspace_bytes);
 
 /*
  * tk_attn_fwd_splitkv -- the same attention for Nq query rows against Nk

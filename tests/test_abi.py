@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol(tk_lib):
 
 
 def test_version_and_status_strings(tk_lib):
-    assert tk_lib.tk_attn_version() == 10500
+    assert tk_lib.tk_attn_version() == 10600
     for code in (0, -1, -2, -3, -4, -5, -6):
         s = tk_lib.tk_attn_status_string(code)
         assert s and s != "unknown status"
@@ -186,3 +186,49 @@ def test_based_rejects_bad_arguments_before_touching_cuda(tk_lib):
     assert chk(y=V + 512) == tk_lib.TK_ATTN_ERR_INVALID_ARG
     assert tk_lib.tk_based_fwd(Q, K, V, O, L, 2, 3, 100, 32, 64, 0.25, 1, 0) == \
         tk_lib.TK_ATTN_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- host-buffer call
+
+W = 6 << 40  # fake device workspace, 256-byte aligned
+
+
+def host_need(B=2, H=3, N=100, D=64):
+    r = lambda x: (x + 255) // 256 * 256
+    return 4 * r(B * H * N * D * 2) + r(B * H * N * 4)
+
+
+def test_host_workspace_bytes(tk_lib):
+    assert tk_lib.tk_attn_fwd_host_workspace_bytes(2, 3, 100, 64) == host_need()
+    assert tk_lib.tk_attn_fwd_host_workspace_bytes(1, 1, 1, 128) == host_need(1, 1, 1, 128)
+    for bad in ((0, 1, 1, 64), (1, 1, 0, 64), (1, 1, 16, 96)):
+        assert tk_lib.tk_attn_fwd_host_workspace_bytes(*bad) == 0
+
+
+def host_check(tk_lib, pieces=0, ws=W, ws_bytes=None, **kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=2, H=3, N=100, D=64, scale=0.125, causal=0)
+    a.update(kw)
+    need = host_need(a["B"], a["H"], a["N"], a["D"]) if ws_bytes is None else ws_bytes
+    return tk_lib.tk_attn_fwd_host_check_args(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"],
+                                              a["H"], a["N"], a["D"], a["scale"], a["causal"],
+                                              pieces, ws, need)
+
+
+def test_host_call_arguments(tk_lib):
+    assert host_check(tk_lib) == tk_lib.TK_ATTN_OK
+    assert host_check(tk_lib, pieces=64, causal=1) == tk_lib.TK_ATTN_OK
+    # the tensor rules of tk_attn_fwd apply to the host buffers
+    assert host_check(tk_lib, D=96) == tk_lib.TK_ATTN_ERR_UNSUPPORTED
+    assert host_check(tk_lib, q=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert host_check(tk_lib, o=V + 16) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    # the pieces count and the workspace
+    assert host_check(tk_lib, pieces=-1) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert host_check(tk_lib, ws=0) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert host_check(tk_lib, ws=W + 16) == tk_lib.TK_ATTN_ERR_INVALID_ARG   # not 256-aligned
+    assert host_check(tk_lib, ws_bytes=host_need() - 1) == tk_lib.TK_ATTN_ERR_INVALID_ARG
+    assert host_check(tk_lib, ws=O - 256) == tk_lib.TK_ATTN_ERR_INVALID_ARG  # over the output
+
+
+def test_host_call_rejects_before_touching_cuda(tk_lib):
+    assert tk_lib.tk_attn_fwd_host(Q, K, V, O, L, 2, 3, 100, 64, 0.125, 0, -1, W, host_need(),
+                                   0) == tk_lib.TK_ATTN_ERR_INVALID_ARG

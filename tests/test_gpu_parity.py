@@ -166,3 +166,41 @@ def test_host_buffer_pieces_match_one_piece(tk_lib):
     o1, l1 = o1.clone(), l1.clone()
     o7, l7 = attention_forward_host(q, k, v, causal=True, chunks=7)  # pieces cut inside batch entries
     assert torch.equal(o1, o7) and torch.equal(l1, l7)
+
+
+@pytest.mark.parametrize("N", [301, 302])
+def test_host_call_odd_lengths_equal_the_device_call(tk_lib, N):
+    # LSE rows of an odd (or 2 mod 4) length start 16-byte aligned only every
+    # 4 (or 2) slices: the pieces are cut there; the result is the device
+    # call's, bit for bit, for every piece count
+    from attention_forward_tk_gb300 import attention_forward, attention_forward_host
+    q, k, v = draw((3, 3, N, 64), seed=12)
+    dev = torch.device("cuda", 0)
+    od, ld = attention_forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    torch.cuda.synchronize()
+    od, ld = od.cpu(), ld.cpu()
+    q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    for pieces in (1, 2, 3, 5, 9):
+        o, l = attention_forward_host(q, k, v, causal=True, chunks=pieces)
+        assert torch.equal(o, od) and torch.equal(l, ld), pieces
+
+
+def test_host_call_pageable_buffers_and_a_side_stream(tk_lib, oracle_lib):
+    # plain (pageable) host tensors through the raw C call on a non-default
+    # stream: the outputs are valid once that stream is synchronised
+    from attention_forward_tk_gb300.api import tk_attn_fwd_host_workspace_bytes
+    B, H, N, D = 2, 3, 260, 128
+    q, k, v = draw((B, H, N, D), seed=13)
+    o = torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16)
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32)
+    dev = torch.device("cuda", 0)
+    ws = torch.empty(tk_attn_fwd_host_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+    st = tk_lib.tk_attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, N, D, 1 / math.sqrt(D), 0, 2,
+                                 ws.data_ptr(), ws.numel(), s.cuda_stream)
+    assert st == 0, tk_lib.tk_attn_status_string(st)
+    s.synchronize()
+    assert tk_lib.tk_attn_last_device_error(s.cuda_stream) == 0
+    o_ref, lse_ref = oracle_lib.attention(q, k, v, 1 / math.sqrt(D), False)
+    compare(o.float().double().numpy(), lse.double().numpy(), o_ref, lse_ref, "pageable host call")
