@@ -10,6 +10,7 @@ GEMM (C = A B^T) on the same TMA / tensor-core pipeline.
 """
 from .api import (  # noqa: F401
     TkAttnError,
+    attention,
     attention_backward,
     attention_forward,
     attention_forward_host,
@@ -24,6 +25,9 @@ from .api import (  # noqa: F401
     tk_attn_bwd_workspace_bytes,
     tk_attn_check_args,
     tk_attn_fwd,
+    tk_attn_fwd_host,
+    tk_attn_fwd_host_check_args,
+    tk_attn_fwd_host_workspace_bytes,
     tk_attn_fwd_qk,
     tk_attn_fwd_splitkv,
     tk_attn_last_device_error,

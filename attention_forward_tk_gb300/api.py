@@ -380,6 +380,43 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
     return dq, dk, dv
 
 
+_autograd_fn = None
+
+
+def _attention_function():
+    """The torch.autograd.Function behind attention(), made on first use (so
+    that importing this module does not import torch)."""
+    global _autograd_fn
+    if _autograd_fn is None:
+        import torch
+
+        class _Attention(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, causal, scale):
+                o, lse = attention_forward(q, k, v, causal, scale)
+                ctx.save_for_backward(q, k, v, o, lse)
+                ctx.causal, ctx.scale = causal, scale
+                return o
+
+            @staticmethod
+            def backward(ctx, dout):
+                q, k, v, o, lse = ctx.saved_tensors
+                dq, dk, dv = attention_backward(q, k, v, o, lse, dout.contiguous(), ctx.causal,
+                                                ctx.scale)
+                return dq, dk, dv, None, None
+
+        _autograd_fn = _Attention
+    return _autograd_fn
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """Differentiable attention for contiguous bf16 CUDA tensors [B, H, N, D]
+    (torch autograd): O from tk_attn_fwd, which also keeps the LSE; dQ, dK,
+    dV from tk_attn_bwd on the saved O and LSE when the graph is
+    differentiated.  Runs on torch's current stream."""
+    return _attention_function().apply(q, k, v, bool(causal), scale)
+
+
 def based_forward(q, k, v, causal: bool = True, scale: float | None = None, out=None, z=None,
                   stream=None, algorithm: str = "auto"):
     """Based linear attention: y, z for bf16 CUDA tensors q, k [B, H, N, 16] and

@@ -133,3 +133,21 @@ def test_bwd_full_size_sampled_slices(tk_lib, oracle_lib, shape):
     got = run_fwd_bwd(tk_lib, q, k, v, do, scale, causal)
     slices = [0, B * H // 3, 2 * B * H // 3 + 1, B * H - 1]
     check(got, oracle_lib.attention_bwd(q, k, v, do, scale, causal, slices=slices), slices)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_autograd_attention(tk_lib, oracle_lib, causal):
+    """attention() under torch autograd: the forward kernel, then the
+    backward kernels on the saved O and LSE, give the oracle's gradients of
+    sum(O * dO)."""
+    from attention_forward_tk_gb300 import attention
+    B, H, N, D = 2, 2, 300, 64
+    q, k, v = draw((B, H, N, D), 21 + int(causal))
+    do = draw_grad((B, H, N, D), 21)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd = (t.to(dev).requires_grad_() for t in (q, k, v))
+    o = attention(qd, kd, vd, causal=causal)
+    (o.float() * do.to(dev).float()).sum().backward()
+    torch.cuda.synchronize()
+    got = [t.grad.float().cpu().double().numpy().reshape(B * H, N, D) for t in (qd, kd, vd)]
+    check(got, oracle_lib.attention_bwd(q, k, v, do, 1.0 / math.sqrt(D), causal))
