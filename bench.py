@@ -483,17 +483,18 @@ def time_e2e(w, steps: int, warmup: int, device):
     for _ in range(warmup):
         step()
     stream = torch.cuda.current_stream(device)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     torch.cuda.synchronize(device)
-    a.record(stream)
-    for _ in range(steps):
+    ev[0].record(stream)
+    for i in range(steps):
         step()
-    b.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize(device)
-    ms = a.elapsed_time(b) / steps
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    ms = ev[0].elapsed_time(ev[steps]) / steps
     h2d = (q.numel() + k.numel() + v.numel()) * 2
     d2h = o.numel() * 2 + lse.numel() * 4
-    return ms, h2d, d2h
+    return ms, h2d, d2h, per_step
 
 
 # ---------------------------------------------------------------- main
@@ -573,8 +574,8 @@ def main():
     t_total, wall = reduce_max([sum(ms) / 1e3, wall], world, device)
     value = job_throughput(world, w.flops, args.steps, t_total)
 
-    e2e_ms, h2d, d2h = (time_e2e(w, max(3, args.steps // 5), 3, device)
-                        if not args.no_e2e else (float("nan"), 0, 0))
+    e2e_ms, h2d, d2h, e2e_steps = (time_e2e(w, max(3, args.steps // 5), 3, device)
+                                   if not args.no_e2e else (float("nan"), 0, 0, []))
     if not args.no_e2e:
         (e2e_ms,) = reduce_max([e2e_ms], world, device)
     e2e_value = job_throughput(world, w.flops, 1, e2e_ms / 1e3)
@@ -695,6 +696,7 @@ def main():
         "e2e": None if args.no_e2e else {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),
+                "ms_steps": [round(x, 3) for x in e2e_steps],
                 "call": "tk_attn_splitkv via torch copies" if w.Nk else
                         "tk_attn_fwd_host (C ABI, pinned host buffers)"},
         "gpu_launches": launches,
