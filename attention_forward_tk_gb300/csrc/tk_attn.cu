@@ -415,12 +415,17 @@ namespace tkattn {
 namespace {
 
 // Ranges for a split over keys: `requested` (> 0), or by default the count
-// that minimises the launch's makespan in K/V steps, rounds x (T + c), when
-// that beats one range by at least 10% (5% with at most 128 queries): units
-// = (slice, query block) pairs x ranges run in ceil(units / SMs) rounds of
-// one unit per SM, and a unit of T tiles costs about c = 3 tiles more for
-// its start and end.  At most one range per 128-key tile, and no empty
-// range: ranges of T tiles, S = ceil(nkv / T).
+// that minimises the launch's makespan in K/V tile steps, when that beats
+// one range by at least 10% (5% with at most 128 queries).  Units = (slice,
+// query block) pairs x ranges run in ceil(units / SMs) rounds of one unit
+// per SM; a unit of T tiles costs about c = 3 tiles more for its start and
+// end, and with more than one range it also writes its rows' fp32 partial O
+// (a block of r <= 256 rows: r / 128 tiles' worth of bytes), which the
+// combine kernel reads back, spread over all SMs.  At most one range per
+// 128-key tile, and no empty range: ranges of T tiles, S = ceil(nkv / T).
+// (Measured on GB300, B1 H32 Nq256 Nk32768: 4 ranges 0.144 ms, 9 ranges
+// 0.148 ms, the count the model chose before it counted the partial
+// results.)
 void resolve_splits(int requested, long long units_q, int nkv, int num_sms, int Nq, int *S,
                     int *T) {
   auto fit = [nkv](long long s, int *S_, int *T_) {
@@ -433,14 +438,18 @@ void resolve_splits(int requested, long long units_q, int nkv, int num_sms, int 
     fit(requested, S, T);
     return;
   }
-  constexpr long long kUnitCost = 3;
+  // costs in 1/128 of a tile step
+  constexpr long long kUnitCost = 3 * 128;
+  const long long rows = Nq < 256 ? Nq : 256;  // query rows a unit holds
   long long best = -1, one = -1;
   for (long long s = 1; s <= nkv && s <= 8LL * num_sms; ++s) {
     int s2, t2;
     fit(s, &s2, &t2);
     if (s2 != s) continue;  // the same ranges as a smaller count
     const long long rounds = (units_q * s2 + num_sms - 1) / num_sms;
-    const long long cost = rounds * (t2 + kUnitCost);
+    const long long partial = s2 > 1 ? rows : 0;
+    const long long combine = s2 > 1 ? s2 * units_q * rows / num_sms : 0;
+    const long long cost = rounds * (128LL * t2 + kUnitCost + partial) + combine;
     if (s2 == 1) one = cost;
     if (best < 0 || cost < best) {
       best = cost;
