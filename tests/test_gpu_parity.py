@@ -204,3 +204,50 @@ def test_host_call_pageable_buffers_and_a_side_stream(tk_lib, oracle_lib):
     assert tk_lib.tk_attn_last_device_error(s.cuda_stream) == 0
     o_ref, lse_ref = oracle_lib.attention(q, k, v, 1 / math.sqrt(D), False)
     compare(o.float().double().numpy(), lse.double().numpy(), o_ref, lse_ref, "pageable host call")
+
+
+def test_host_call_from_two_threads(tk_lib):
+    # two host threads, each with its own buffers, workspace and stream, call
+    # the host-buffer entry point at once: the per-device copy streams and
+    # events are shared, and each result is the device call's
+    import threading
+
+    from attention_forward_tk_gb300 import attention_forward
+    from attention_forward_tk_gb300.api import tk_attn_fwd_host_workspace_bytes
+    dev = torch.device("cuda", 0)
+    B, H, N, D = 2, 4, 640, 128
+    inputs = [draw((B, H, N, D), seed=30 + t) for t in range(2)]
+    expect = []
+    for q, k, v in inputs:
+        o, l = attention_forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
+        torch.cuda.synchronize()
+        expect.append((o.cpu(), l.cpu()))
+    results, errors = [None, None], []
+
+    def worker(t):
+        try:
+            q, k, v = (x.pin_memory() for x in inputs[t])
+            o = torch.empty((B, H, N, D), dtype=torch.bfloat16, pin_memory=True)
+            l = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+            ws = torch.empty(tk_attn_fwd_host_workspace_bytes(B, H, N, D), dtype=torch.uint8,
+                             device=dev)
+            s = torch.cuda.Stream(dev)
+            for _ in range(5):
+                st = tk_lib.tk_attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             o.data_ptr(), l.data_ptr(), B, H, N, D,
+                                             1 / math.sqrt(D), 1, 3, ws.data_ptr(), ws.numel(),
+                                             s.cuda_stream)
+                assert st == 0, st
+            s.synchronize()
+            results[t] = (o.clone(), l.clone())
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t in range(2):
+        assert torch.equal(results[t][0], expect[t][0]) and torch.equal(results[t][1], expect[t][1])
