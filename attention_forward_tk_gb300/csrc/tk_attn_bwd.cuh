@@ -171,6 +171,24 @@ __device__ __forceinline__ void causal_section(const BwdParams &p, int u, int &b
   bh = section * p.head_group + rr % g;
 }
 
+// The uc-th unit of this CTA, or -1 when none is left: causal launches
+// carry each CTA's list, built on the host greedily in the unit order (the
+// next unit to the CTA with the fewest tile steps so far, as for the
+// forward's SchedTable); otherwise, and when the list does not fit, the
+// stride order.
+template <bool kCausal>
+__device__ __forceinline__ int bwd_unit_at(const SchedFor<kCausal> &tab, const BwdParams &p,
+                                           int uc) {
+  if constexpr (kCausal) {
+    if (tab.n > 0) {
+      const int i = tab.off[blockIdx.x] + uc;
+      return i < tab.off[blockIdx.x + 1] ? (int)tab.units[i] : -1;
+    }
+  }
+  const int u = blockIdx.x + uc * (int)gridDim.x;
+  return u < p.num_units ? u : -1;
+}
+
 template <bool kCausal>
 __device__ __forceinline__ void dkdv_unit(const BwdParams &p, int u, int &bh, int &j, int &i0,
                                           int &n) {
@@ -215,7 +233,8 @@ __global__ void __launch_bounds__(576, 1)
     tk_attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v,
-                            const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                            const __grid_constant__ CUtensorMap tm_do, const BwdParams p,
+                            const __grid_constant__ SchedFor<kCausal> tab) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdShared<C::kStages> sb;
@@ -262,7 +281,8 @@ __global__ void __launch_bounds__(576, 1)
     const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t it = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = bwd_unit_at<kCausal>(tab, p, 0); u >= 0 && ok;
+         u = bwd_unit_at<kCausal>(tab, p, (int)++uc)) {
       int bh, j, i0, n;
       dkdv_unit<kCausal>(p, u, bh, j, i0, n);
       const int kj = j * 128 + r;
@@ -389,7 +409,8 @@ __global__ void __launch_bounds__(576, 1)
     // ---------------------------------------------------------- TMA producer
     uint32_t it = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = bwd_unit_at<kCausal>(tab, p, 0); u >= 0 && ok;
+         u = bwd_unit_at<kCausal>(tab, p, (int)++uc)) {
       int bh, j, i0, n;
       dkdv_unit<kCausal>(p, u, bh, j, i0, n);
       if (uc > 0 && !mbar_wait(&sb.fix_empty, (uc - 1) & 1, abort_flag)) {
@@ -435,7 +456,8 @@ __global__ void __launch_bounds__(576, 1)
     uint32_t it = 0, uc = 0;
     bool ok = true;
     auto stage_q = [&](uint32_t t) { return smem_addr(ring + (t % C::kStages) * 2 * C::kTileBytes); };
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = bwd_unit_at<kCausal>(tab, p, 0); u >= 0 && ok;
+         u = bwd_unit_at<kCausal>(tab, p, (int)++uc)) {
       int bh, j, i0, n;
       dkdv_unit<kCausal>(p, u, bh, j, i0, n);
       if (!mbar_wait(&sb.fix_full, uc & 1, abort_flag) ||
@@ -546,7 +568,8 @@ __global__ void __launch_bounds__(576, 1)
     tk_attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
-                          const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                          const __grid_constant__ CUtensorMap tm_do, const BwdParams p,
+                          const __grid_constant__ SchedFor<kCausal> tab) {
   using C = BwdCfg<D>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -600,7 +623,8 @@ __global__ void __launch_bounds__(576, 1)
     const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
     uint32_t it = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = bwd_unit_at<kCausal>(tab, p, 0); u >= 0 && ok;
+         u = bwd_unit_at<kCausal>(tab, p, (int)++uc)) {
       int bh, i, n;
       dq_unit<kCausal>(p, u, bh, i, n);
       const int qi = i * 128 + r;
@@ -707,7 +731,8 @@ __global__ void __launch_bounds__(576, 1)
     // ---------------------------------------------------------- TMA producer
     uint32_t it = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = bwd_unit_at<kCausal>(tab, p, 0); u >= 0 && ok;
+         u = bwd_unit_at<kCausal>(tab, p, (int)++uc)) {
       int bh, i, n;
       dq_unit<kCausal>(p, u, bh, i, n);
       if (uc > 0 && !mbar_wait(&sb.fix_empty, (uc - 1) & 1, abort_flag)) {
@@ -756,7 +781,8 @@ __global__ void __launch_bounds__(576, 1)
     auto v_addr = [&](uint32_t t) { return smem_addr(vring + (t % VS) * C::kTileBytes); };
     uint32_t it = 0, uc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+    for (int u = bwd_unit_at<kCausal>(tab, p, 0); u >= 0 && ok;
+         u = bwd_unit_at<kCausal>(tab, p, (int)++uc)) {
       int bh, i, n;
       dq_unit<kCausal>(p, u, bh, i, n);
       // S_0 = Q K_0^T (rows: queries; columns: keys)
