@@ -442,10 +442,15 @@ def bwd_flops(w) -> float:
 
 def time_e2e(w, steps: int, warmup: int, device):
     """The same call from pinned host buffers: H2D of Q, K, V, the kernel, and
-    D2H of O and LSE every step, timed with CUDA events around all of it."""
+    D2H of O and LSE every step, timed with CUDA events around all of it.
+    The steps are enqueued back to back, as a caller pipelining its calls
+    would (each call's copies start only after the previous call's last
+    copy-out, so the steps do not overlap), and the stream is synchronised
+    once at the end: a host-side pause between two calls does not idle the
+    GPU while work is queued."""
     import torch
 
-    from attention_forward_tk_gb300 import attention_forward_host
+    from attention_forward_tk_gb300 import api
     from attention_forward_tk_gb300.inputs import workload_inputs
 
     q, k, v = (t.cpu().pin_memory() for t in workload_inputs(w, device=device))
@@ -470,16 +475,19 @@ def time_e2e(w, steps: int, warmup: int, device):
             attention_forward_splitkv(qd, kd, vd, w.scale, 0, od, ld, ws, causal=w.causal)
             o.copy_(od, non_blocking=True)
             lse.copy_(ld, non_blocking=True)
-            torch.cuda.current_stream(device).synchronize()
     else:
         # the C call with host buffers (tk_attn_fwd_host): copies pipelined
         # with the kernel inside the library
-        from attention_forward_tk_gb300.api import tk_attn_fwd_host_workspace_bytes
-        ws = torch.empty(tk_attn_fwd_host_workspace_bytes(w.B, w.H, w.N, w.D), dtype=torch.uint8,
-                         device=device)
+        ws = torch.empty(api.tk_attn_fwd_host_workspace_bytes(w.B, w.H, w.N, w.D),
+                         dtype=torch.uint8, device=device)
+        handle = torch.cuda.current_stream(device).cuda_stream
 
         def step():
-            attention_forward_host(q, k, v, w.causal, w.scale, ws, o, lse)
+            st = api.tk_attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), w.B, w.H, w.N, w.D, w.scale,
+                                      int(w.causal), 0, ws.data_ptr(), ws.numel(), handle)
+            if st != 0:
+                raise RuntimeError(f"tk_attn_fwd_host: {api.tk_attn_status_string(st)}")
     for _ in range(warmup):
         step()
     stream = torch.cuda.current_stream(device)
