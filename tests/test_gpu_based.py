@@ -10,7 +10,6 @@ sums z from the unrounded fp32 T, and rounds y to bf16 once.  So
 
 and the relative RMS error of y must stay below 2^-6.
 """
-import math
 
 import numpy as np
 import pytest
