@@ -151,3 +151,16 @@ def test_autograd_attention(tk_lib, oracle_lib, causal):
     torch.cuda.synchronize()
     got = [t.grad.float().cpu().double().numpy().reshape(B * H, N, D) for t in (qd, kd, vd)]
     check(got, oracle_lib.attention_bwd(q, k, v, do, 1.0 / math.sqrt(D), causal))
+
+
+def test_bwd_causal_beyond_the_unit_lists(tk_lib, oracle_lib):
+    """More causal units (B2 H100 N8192: 200 slices x 64 tiles = 12,800) than
+    the per-CTA unit lists hold: the kernels fall back to the stride order.
+    Two slices checked in full."""
+    B, H, N, D = 2, 100, 8192, 64
+    q, k, v = draw((B, H, N, D), 5)
+    do = draw_grad((B, H, N, D), 5)
+    scale = 1.0 / math.sqrt(D)
+    got = run_fwd_bwd(tk_lib, q, k, v, do, scale, True)
+    slices = [7, B * H - 1]
+    check(got, oracle_lib.attention_bwd(q, k, v, do, scale, True, slices=slices), slices)
